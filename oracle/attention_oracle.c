@@ -1,0 +1,180 @@
+/*
+ * Oracle for exact (softmax) attention — TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, obviously correct fp64 CPU restatement of what the fused
+ * attention forward computes.  Only tests/, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library; the product path
+ * never does.  It shares no code, header or constant with the CUDA path.
+ *
+ * Definition followed (no tiling, no online rescaling, no fusion):
+ *   "Parsing FlashAttention (2): FlashAttention-v1 forward pass", §1.1
+ *   (S = Q K^T, P = softmax(S), O = P V) and §2.1 eqs (1)-(5) (safe softmax);
+ *   "Online Softmax and FlashAttention" (course unit 12), causal-mask passage
+ *   (M_ij = -inf for j > i, future weights exactly 0).
+ * Readings of points the pages leave open:
+ *   - the scale multiplies the fp64 dot product (it is not folded into Q);
+ *   - LSE_i = m_i + ln(l_i) of the scaled, masked scores (natural log);
+ *   - causal masking is square and top-left aligned (query i sees keys 0..i).
+ *
+ * Inputs are bf16 bit patterns (uint16); each is widened to fp64 exactly.
+ * Every floating-point step below runs in fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of a bf16 bit pattern: bf16 is the top half of an fp32. */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One row of scores (page 1 §1.1; page 2 causal passage):
+ *   s_j = scale * sum_t q_t * k_{j,t}     for visible j,
+ *   s_j = -inf                           for j > i when causal.
+ * q_row: d bf16 values of query i; k: n_keys x d bf16 row-major.
+ */
+void oracle_score_row(const uint16_t *q_row, const uint16_t *k, int64_t i,
+                      int64_t n_keys, int64_t d, double scale, int causal,
+                      double *s)
+{
+    for (int64_t j = 0; j < n_keys; ++j) {
+        if (causal && j > i) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t)
+            dot += oracle_bf16_to_double(q_row[t]) *
+                   oracle_bf16_to_double(k[j * d + t]);
+        s[j] = scale * dot;
+    }
+}
+
+/*
+ * Safe softmax of one vector (page 1 §2.1, eqs (1)-(5)):
+ *   m = max_j x_j,  shifted_j = x_j - m,  f_j = exp(shifted_j),
+ *   l = sum_j f_j,  p_j = f_j / l.
+ * Entries equal to -inf give f_j = exp(-inf) = 0 exactly.  Any output
+ * pointer may be NULL.  Requires at least one finite entry.
+ */
+void oracle_safe_softmax(const double *x, int64_t n, double *shifted,
+                         double *p, double *m_out, double *l_out)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j)
+        if (x[j] > m) m = x[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double sh = x[j] - m;
+        if (shifted) shifted[j] = sh;
+        l += exp(sh);
+    }
+    if (p)
+        for (int64_t j = 0; j < n; ++j) p[j] = exp(x[j] - m) / l;
+    if (m_out) *m_out = m;
+    if (l_out) *l_out = l;
+}
+
+/*
+ * Full score block for rows [0, nq) of q against all nk keys; row r of q is
+ * query index row_offset + r (used only by the causal test j > i).
+ * s_out: nq x nk, row-major.
+ */
+void oracle_scores(const uint16_t *q, const uint16_t *k, int64_t nq,
+                   int64_t nk, int64_t d, double scale, int causal,
+                   int64_t row_offset, double *s_out)
+{
+    for (int64_t r = 0; r < nq; ++r)
+        oracle_score_row(q + r * d, k, row_offset + r, nk, d, scale, causal,
+                         s_out + r * nk);
+}
+
+/*
+ * Attention forward for selected rows of every (batch, head) slice.
+ *   q, k, v : [BH][N][d] bf16 bit patterns
+ *   rows    : n_rows query indices (each in [0, N)), applied to every slice;
+ *             NULL means all rows (n_rows must then equal N)
+ *   o_out   : [BH][n_rows][d] fp64,   O_i = sum_j P_ij v_j
+ *   lse_out : [BH][n_rows]   fp64,   LSE_i = m_i + ln(l_i)
+ *   p_out   : optional [BH][n_rows][N] fp64 probabilities (may be NULL)
+ * Returns 0, or -1 on bad arguments / -2 on allocation failure.
+ */
+int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t BH, int64_t N, int64_t d, int causal,
+                     double scale, const int64_t *rows, int64_t n_rows,
+                     double *o_out, double *lse_out, double *p_out,
+                     int n_threads)
+{
+    if (!q || !k || !v || !o_out || !lse_out) return -1;
+    if (BH <= 0 || N <= 0 || d <= 0 || n_rows <= 0) return -1;
+    if (!rows && n_rows != N) return -1;
+    for (int64_t r = 0; rows && r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+
+    int failed = 0;
+    int64_t tasks = BH * n_rows;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel
+#endif
+    {
+        double *s = (double *)malloc((size_t)N * sizeof(double));
+        double *p = (double *)malloc((size_t)N * sizeof(double));
+        if (!s || !p) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+        for (int64_t task = 0; task < tasks; ++task) {
+            if (!s || !p) continue;
+            int64_t bh = task / n_rows;
+            int64_t r = task % n_rows;
+            int64_t i = rows ? rows[r] : r;
+            const uint16_t *qh = q + (bh * N + i) * d;
+            const uint16_t *kh = k + bh * N * d;
+            const uint16_t *vh = v + bh * N * d;
+
+            oracle_score_row(qh, kh, i, N, d, scale, causal, s);
+            double m, l;
+            oracle_safe_softmax(s, N, NULL, p, &m, &l);
+
+            double *o = o_out + (bh * n_rows + r) * d;
+            for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                if (p[j] == 0.0) continue; /* masked keys add 0 * v_j */
+                for (int64_t t = 0; t < d; ++t)
+                    o[t] += p[j] * oracle_bf16_to_double(vh[j * d + t]);
+            }
+            lse_out[bh * n_rows + r] = m + log(l);
+            if (p_out)
+                memcpy(p_out + (bh * n_rows + r) * N, p,
+                       (size_t)N * sizeof(double));
+        }
+        free(s);
+        free(p);
+    }
+    return failed ? -2 : 0;
+}
+
+/* Threads OpenMP would use by default (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
