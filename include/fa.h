@@ -1,0 +1,108 @@
+/*
+ * fa.h — C ABI of the fused attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * Operation (one call = every batch and head):
+ *
+ *   S   = scale * Q K^T                      ("Parsing FlashAttention (2):
+ *   S_ij = -inf for j > i when causal          FlashAttention-v1 forward pass",
+ *   O   = softmax_row(S) V                     §1.1 and §2.1 eqs (1)-(5);
+ *   LSE_i = ln sum_j exp(S_ij)                 causal mask as in "Online Softmax
+ *                                              and FlashAttention", course unit 12)
+ *
+ * computed by the tiled online softmax of the same pages (running max m,
+ * running exponent sum l, accumulator rescaled by exp(m_old - m_new)), so no
+ * N x N score or probability matrix is ever written to device memory.
+ * LSE_i = m_i + ln(l_i) is the single statistic that summarises (m, l) for a
+ * later backward pass (page 1 §1.2(3), "recomputation").
+ *
+ * Conventions for every entry point:
+ *  - Pointers named q, k, v, o, lse are DEVICE pointers; nothing is copied to
+ *    or from the host.  The caller owns all buffers; the library allocates no
+ *    device memory and keeps no per-call state.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream): they return after enqueueing and never synchronise.
+ *  - Errors are reported by return code (FA_OK on success).  Arguments are
+ *    validated before anything is enqueued; on error nothing is launched and
+ *    the outputs are untouched.  No C++ exception crosses this boundary.
+ *  - Thread-safe: concurrent calls from several host threads are allowed.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum fa_status {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,      /* a required pointer is NULL */
+  FA_ERR_SHAPE = 2,     /* B, H or N <= 0, or B*H*N*d overflows the index space */
+  FA_ERR_HEAD_DIM = 3,  /* d is not 64 or 128 */
+  FA_ERR_ALIGN = 4,     /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+  FA_ERR_SCALE = 5,     /* scale is NaN or infinite */
+  FA_ERR_ALIAS = 6,     /* o or lse overlaps an input, or o overlaps lse */
+  FA_ERR_DEVICE = 7,    /* current device is not compute capability 10.3 (sm_103a) */
+  FA_ERR_LAUNCH = 8,    /* CUDA runtime / driver error while preparing or launching */
+  FA_ERR_TIMEOUT = 9    /* a kernel wait exceeded its limit (see fa_get_device_status) */
+};
+
+/*
+ * fa_fwd — attention forward for all (batch, head) slices.
+ *
+ *   q, k, v : const bf16 [B][H][N][d], contiguous, 16-byte aligned (device)
+ *   o       : bf16 [B][H][N][d], contiguous, 16-byte aligned (device), written
+ *   lse     : fp32 [B][H][N], contiguous (device), written; natural-log units
+ *             of the scaled, masked scores: LSE_i = ln sum_j exp(S_ij)
+ *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1
+ *   d       : head dimension, 64 or 128
+ *   causal  : 0 = full attention, 1 = query i sees keys 0..i (square,
+ *             top-left aligned)
+ *   scale   : any finite float multiplying Q K^T (typically 1/sqrt(d))
+ *   stream  : cudaStream_t to enqueue on
+ *
+ * Inputs are read, never modified; o and lse must not overlap q, k, v or each
+ * other.  Arithmetic: bf16 operands, fp32 accumulation and softmax
+ * statistics, bf16 probabilities in the P.V product, bf16 output rounded to
+ * nearest even.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
+           int d, int causal, float scale, void *stream);
+
+/* Human-readable text for a return code (static storage, never NULL). */
+const char *fa_strerror(int code);
+
+/*
+ * Device status word of the kernels on the current device: a bit set of
+ * FA_DEVICE_STATUS_* values, sticky until fa_clear_device_status().  Reading
+ * it synchronises the current device (it copies one word to the host).
+ * Returns FA_OK or FA_ERR_LAUNCH; *status must not be NULL (FA_ERR_NULL).
+ */
+#define FA_DEVICE_STATUS_TIMEOUT 1u
+int fa_get_device_status(unsigned int *status);
+int fa_clear_device_status(void);
+
+/*
+ * Upper bound, in nanoseconds, on any single wait inside the kernels
+ * (default 1e9).  A wait that exceeds it sets FA_DEVICE_STATUS_TIMEOUT, the
+ * kernel abandons its work (outputs undefined), frees its on-chip resources
+ * and exits.  0 restores the default.  Applies to later calls, process-wide.
+ */
+int fa_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Test hook: a bit set of FA_INJECT_* faults applied by later calls,
+ * process-wide (0 = none, the default).  FA_INJECT_SKIP_FIRST_V_LOAD makes
+ * every CTA skip its first V-tile copy, so a wait runs out and the call ends
+ * with FA_DEVICE_STATUS_TIMEOUT set.  For tests of the failure path only.
+ */
+#define FA_INJECT_SKIP_FIRST_V_LOAD 1u
+int fa_set_fault_injection(unsigned int flags);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

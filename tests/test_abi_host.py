@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched):
+the library builds and loads, exports every function include/fa.h declares,
+and rejects bad arguments with the documented codes before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+# Codes from include/fa.h
+FA_OK, FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_ALIGN = 0, 1, 2, 3, 4
+FA_ERR_SCALE, FA_ERR_ALIAS, FA_ERR_DEVICE, FA_ERR_LAUNCH = 5, 6, 7, 8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import tiled_attention_forward_attn_gb300 as fa
+    from tiled_attention_forward_attn_gb300 import _build
+
+    _build.build()
+    return fa.load_library()
+
+
+def _declared_functions():
+    names = []
+    for fname in sorted(os.listdir(HEADER_DIR)):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("fa_fwd", "fa_strerror", "fa_get_device_status", "fa_clear_device_status",
+                     "fa_set_wait_limit_ns", "fa_set_fault_injection", "fa_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in include/*.h but not exported: {missing}"
+
+
+def test_strerror_and_version(lib):
+    for code in range(0, 10):
+        assert isinstance(lib.fa_strerror(code), bytes) and lib.fa_strerror(code)
+    assert lib.fa_strerror(12345) == b"unknown error code"
+    assert lib.fa_version() >= 100
+
+
+A16 = 0x10000  # fake, 16-byte aligned addresses (never dereferenced)
+
+
+def _call(lib, q=A16, k=2 * A16, v=3 * A16, o=4 * A16, lse=5 * A16, B=1, H=1, N=128, d=64,
+          causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_null_pointers_rejected(lib, which):
+    assert _call(lib, **{which: 0}) == FA_ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0), dict(B=-1), dict(N=-5),
+                                dict(causal=2), dict(B=65536, H=65536),
+                                dict(N=65536 * 128 + 1)])
+def test_bad_shapes_rejected(lib, kw):
+    assert _call(lib, **kw) == FA_ERR_SHAPE
+
+
+@pytest.mark.parametrize("d", [0, 16, 32, 96, 127, 256])
+def test_unsupported_head_dim_rejected(lib, d):
+    assert _call(lib, d=d) == FA_ERR_HEAD_DIM
+
+
+@pytest.mark.parametrize("kw", [dict(q=A16 + 2), dict(k=2 * A16 + 8), dict(v=3 * A16 + 1),
+                                dict(o=4 * A16 + 4), dict(lse=5 * A16 + 2)])
+def test_misaligned_pointers_rejected(lib, kw):
+    assert _call(lib, **kw) == FA_ERR_ALIGN
+
+
+@pytest.mark.parametrize("scale", [float("nan"), float("inf"), float("-inf")])
+def test_non_finite_scale_rejected(lib, scale):
+    assert _call(lib, scale=scale) == FA_ERR_SCALE
+
+
+def test_aliasing_outputs_rejected(lib):
+    # o == q
+    assert _call(lib, o=A16) == FA_ERR_ALIAS
+    # lse inside v (v spans 128*64*2 bytes)
+    assert _call(lib, lse=3 * A16 + 1024) == FA_ERR_ALIAS
+    # lse inside o
+    assert _call(lib, lse=4 * A16 + 64) == FA_ERR_ALIAS
+
+
+def test_valid_arguments_without_a_device_report_an_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present; covered by the GPU tests")
+    assert _call(lib) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
+def test_python_binding_validates_before_calling(lib):
+    torch = pytest.importorskip("torch")
+    import tiled_attention_forward_attn_gb300 as fa
+
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, TypeError)):
+        fa.fa_fwd(q, q, q, q.clone(), torch.zeros(1, 1, 8), False, 0.1)  # CPU tensors
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q[:, :, :4], q, q.clone(), torch.zeros(1, 1, 8), False, 0.1)
+
+
+def test_status_hooks_accept_arguments(lib):
+    assert lib.fa_set_wait_limit_ns(ctypes.c_ulonglong(0)) == FA_OK
+    assert lib.fa_set_fault_injection(0) == FA_OK
+    assert lib.fa_get_device_status(None) == FA_ERR_NULL

@@ -1,0 +1,171 @@
+"""Fused attention forward for GB300 (sm_103a) — Python binding.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libfa.so`` behind the C ABI of ``include/fa.h``.  There is no
+CPU or PyTorch fallback; if the library is missing, every call raises.
+
+Names follow the C ABI: :func:`fa_fwd` takes preallocated device tensors;
+:func:`attention_forward` allocates the outputs and calls :func:`fa_fwd`.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version",
+    "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
+    "fa_set_fault_injection", "load_library", "LIB_PATH",
+    "FA_DEVICE_STATUS_TIMEOUT", "FA_INJECT_SKIP_FIRST_V_LOAD",
+]
+
+LIB_PATH = _build.LIB_PATH
+FA_DEVICE_STATUS_TIMEOUT = 1
+FA_INJECT_SKIP_FIRST_V_LOAD = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A non-zero return code from the C ABI."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: error {code}: {fa_strerror(code)}")
+
+
+def load_library(path: str | None = None):
+    """Load libfa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not built: {path} is missing "
+                "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.restype = i
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        lib.fa_strerror.restype = ctypes.c_char_p
+        lib.fa_strerror.argtypes = [i]
+        lib.fa_get_device_status.restype = i
+        lib.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.fa_clear_device_status.restype = i
+        lib.fa_clear_device_status.argtypes = []
+        lib.fa_set_wait_limit_ns.restype = i
+        lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_set_fault_injection.restype = i
+        lib.fa_set_fault_injection.argtypes = [ctypes.c_uint]
+        lib.fa_version.restype = i
+        lib.fa_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def fa_strerror(code: int) -> str:
+    return load_library().fa_strerror(int(code)).decode()
+
+
+def fa_version() -> int:
+    return int(load_library().fa_version())
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise FAError(code, where)
+
+
+def fa_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+               N: int, d: int, causal: bool, scale: float, stream: int = 0) -> int:
+    """Direct call with integer device addresses; returns the C return code."""
+    return int(load_library().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N),
+                                     int(d), int(bool(causal)), float(scale), stream or None))
+
+
+def _dims(t):
+    if t.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    return tuple(int(x) for x in t.shape)
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """Attention forward into preallocated CUDA tensors.
+
+    q, k, v, o: ``torch.bfloat16`` ``[B, H, N, d]`` contiguous on one CUDA
+    device; lse: ``torch.float32`` ``[B, H, N]``.  Enqueued on ``stream``
+    (default: the current torch stream of q's device); asynchronous.
+    """
+    import torch
+
+    B, H, N, d = _dims(q)
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(B, H, N, d)}")
+    if tuple(lse.shape) != (B, H, N):
+        raise ValueError(f"lse has shape {tuple(lse.shape)}, expected {(B, H, N)}")
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != q.device:
+            raise ValueError("all tensors must be on one device")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        _check(fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, N, d, causal, scale, handle), "fa_fwd")
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate ``O`` (bf16) and ``LSE`` (fp32) and run :func:`fa_fwd`.
+
+    ``scale`` defaults to ``1/sqrt(d)``.  Returns ``(O, LSE)``.
+    """
+    import torch
+
+    B, H, N, d = _dims(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def fa_get_device_status() -> int:
+    """Sticky device status bits of the current device (synchronises it)."""
+    st = ctypes.c_uint(0)
+    _check(load_library().fa_get_device_status(ctypes.byref(st)), "fa_get_device_status")
+    return int(st.value)
+
+
+def fa_clear_device_status() -> None:
+    _check(load_library().fa_clear_device_status(), "fa_clear_device_status")
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    _check(load_library().fa_set_wait_limit_ns(int(ns)), "fa_set_wait_limit_ns")
+
+
+def fa_set_fault_injection(flags: int) -> None:
+    _check(load_library().fa_set_fault_injection(int(flags)), "fa_set_fault_injection")
+
+
+def nominal_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
+    """4·B·H·N²·d, halved when causal (the metric's nominal count)."""
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f

@@ -1,0 +1,194 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, TMA
+// descriptor construction and the launch of the fused attention kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<unsigned int> g_inject{0u};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+// Per-device readiness: 0 = unchecked, 1 = supported and configured, -1 = unsupported.
+std::mutex g_dev_mutex;
+int g_dev_state[kMaxDevices] = {0};
+
+void load_encode() {
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  void* fn = nullptr;
+  g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                  cudaEnableDefault, &q);
+  if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess && fn != nullptr)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+template <int D>
+cudaError_t configure_kernel() {
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::Cfg<D>::kSmemAlloc));
+}
+
+// Checks that the current device is sm_103 and configures the kernels for it once.
+int prepare_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_dev_state[dev] == 1) return FA_OK;
+  if (g_dev_state[dev] == -1) return FA_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  if (major != 10 || minor != 3) {
+    g_dev_state[dev] = -1;
+    return FA_ERR_DEVICE;
+  }
+  if (configure_kernel<64>() != cudaSuccess || configure_kernel<128>() != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  g_dev_state[dev] = 1;
+  return FA_OK;
+}
+
+// [BH][N][d] bf16 viewed as a 3-D tensor (d innermost), boxes of
+// 64 columns x 128 rows x 1 slice with the 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r =
+      g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+template <int D>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+           const CUtensorMap& mo, const fa::FwdParams& prm, int BH, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(prm.num_q_tiles));
+  fa::fa_fwd_kernel<D>
+      <<<grid, fa::kNumThreads, fa::Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, mo, prm);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int N, int d, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t num_q_tiles = (static_cast<int64_t>(N) + fa::kBlockM - 1) / fa::kBlockM;
+  // grid.x = B*H (<= 2^31-1), grid.y = query tiles (<= 65535); element
+  // offsets bh*N + row must fit in int for the LSE store.
+  if (BH > INT_MAX || num_q_tiles > 65535 || BH * N > INT_MAX) return FA_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) &
+      15u)
+    return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
+  const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
+  for (const void* in : {q, k, v}) {
+    if (overlaps(o, tensor_bytes, in, tensor_bytes) || overlaps(lse, lse_bytes, in, tensor_bytes))
+      return FA_ERR_ALIAS;
+  }
+  if (overlaps(o, tensor_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+
+  int dev = 0;
+  const int prep = prepare_device(&dev);
+  if (prep != FA_OK) return prep;
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return FA_ERR_LAUNCH;
+
+  CUtensorMap mq, mk, mv, mo;
+  if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
+      !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
+      !encode_map(&mv, v, static_cast<int>(BH), N, d) ||
+      !encode_map(&mo, o, static_cast<int>(BH), N, d))
+    return FA_ERR_LAUNCH;
+
+  fa::FwdParams prm;
+  prm.lse = lse;
+  prm.N = N;
+  prm.num_q_tiles = static_cast<int>(num_q_tiles);
+  prm.causal = causal;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.inject = g_inject.load(std::memory_order_relaxed);
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 64) return launch<64>(mq, mk, mv, mo, prm, static_cast<int>(BH), s);
+  return launch<128>(mq, mk, mv, mo, prm, static_cast<int>(BH), s);
+}
+
+extern "C" const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "success";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and within index limits; causal 0 or 1)";
+    case FA_ERR_HEAD_DIM: return "unsupported head dimension (d must be 64 or 128)";
+    case FA_ERR_ALIGN: return "misaligned pointer (q, k, v, o need 16 bytes; lse needs 4)";
+    case FA_ERR_SCALE: return "scale is not finite";
+    case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
+    case FA_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+    case FA_ERR_LAUNCH: return "CUDA error while preparing or launching the kernel";
+    case FA_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
+    default: return "unknown error code";
+  }
+}
+
+extern "C" int fa_get_device_status(unsigned int* status) {
+  if (!status) return FA_ERR_NULL;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof v) != cudaSuccess) return FA_ERR_LAUNCH;
+  *status = v;
+  return FA_OK;
+}
+
+extern "C" int fa_clear_device_status(void) {
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof zero) == cudaSuccess ? FA_OK
+                                                                               : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+extern "C" int fa_set_fault_injection(unsigned int flags) {
+  g_inject.store(flags, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+extern "C" int fa_version(void) { return 100; }
