@@ -1,0 +1,346 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+Default workload: B=2, H=16, N=4096, d=128, causal, bf16 (the headline
+configuration).  One step = one fa_fwd call over the whole batch (every
+(batch, head, query tile) unit).  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl ours (default): CUDA-event time of K launches with inputs resident in
+HBM and L2 flushed (a 256 MiB write) between launches; the end-to-end
+figure adds, every step, the pinned-host -> device copy of Q, K, V and the
+device -> host copy of O and LSE.  --impl reference: the fp64 CPU oracle on
+a fixed seeded sample of query rows of the same workload (the baseline
+program), on the host cores.  Under torchrun each rank runs the workload on
+its own GPU (independent replicas: weak scaling); timing is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOPS & % of GB300 BF16 tensor peak (N=4096,d=128,causal)"
+UNIT = "TFLOPS"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+# Per-launch DRAM traffic of the attention kernel on this workload, from an
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum); None until the
+# kernel it was taken on is the one benchmarked.
+NCU_TRAFFIC_BYTES = None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._reader.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        rows = [(t, l.split(", ")) for t, l in self.lines if l]
+        inside = [r for t, r in rows if self.t_start is not None and self.t_start <= t <= self.t_stop]
+        use = inside if inside else rows
+        if not use:
+            return None
+        sm = [float(r[1]) for r in use if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        sm_max = [float(r[2]) for r in use if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        for r in use:
+            if len(r) < 9:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(sm_max) if sm_max else None,
+                "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, qkv, rows_per_head: int, seed: int, threads: int = 0):
+    """Time the fp64 oracle on a fixed seeded sample of query rows.
+
+    Returns (seconds, flops, rows, cores).  FLOPs count the same work the
+    metric counts: 4·d per (query, visible key) pair (2·d for the score,
+    2·d for the P·V row)."""
+    import oracle
+
+    q, k, v = qkv
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = np.sort(rng.permutation(w.N)[:rows_per_head]).astype(np.int64)
+    visible = (rows + 1) if w.causal else np.full(rows.size, w.N)
+    flops = float(4.0 * w.d * visible.sum() * w.B * w.H)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, flops, rows.size, oracle.max_threads() if threads <= 0 else threads
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    rows_per_head = args.ref_rows
+    qkv = workloads.generate(w)
+    times = []
+    flops = 0.0
+    cores = 0
+    for i in range(args.warmup + args.steps):
+        dt, flops, n_rows, cores = cpu_oracle_sample(w, qkv, rows_per_head, seed=1000 + w.seed)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = (f"{rows_per_head} seeded query rows per head x {w.B * w.H} heads "
+              f"({100.0 * rows_per_head / w.N:.2f}% of the rows) per step, fp64 oracle, "
+              f"{cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+
+    import tiled_attention_forward_attn_gb300 as fa
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load_library()
+
+    q, k, v = workloads.generate(w)
+    qd, kd, vd = (workloads.as_torch_bf16(a).to(dev) for a in (q, k, v))
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_stop()
+    if world > 1:
+        torch.distributed.barrier()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(per_launch_ms)
+    clocks = sampler.stop() if sampler else None
+
+    # End to end through the same C ABI: pinned host inputs -> device,
+    # attention, device -> pinned host outputs, every step.
+    hq, hk, hv = (workloads.as_torch_bf16(a).pin_memory() for a in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = 3 * hq.numel() * hq.element_size()
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(10, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([kernel_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        kernel_ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank == 0:
+        peaks, peaks_src = load_peaks()
+        flops_step = w.flops
+        value = world * flops_step * args.steps / (kernel_ms * 1e-3) / 1e12
+        avg_launch_s = kernel_ms * 1e-3 / args.steps
+        achieved = flops_step / avg_launch_s / 1e12
+        peak = float(peaks["bf16_tflops"])
+        e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+        cpu = None
+        if world == 1 and not args.skip_cpu_baseline:
+            rows = args.cpu_rows
+            dt, fl, n_rows, cores = cpu_oracle_sample(w, (q, k, v), rows, seed=2000 + w.seed)
+            cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": (f"{n_rows} seeded query rows per head x {w.B * w.H} heads "
+                              f"({100.0 * n_rows / w.N:.2f}% of the rows), fp64 oracle, "
+                              f"{dt:.1f} s")}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": kernel_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "scale": w.scale,
+                       "l2": "flushed between launches (256 MiB write, untimed)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peaks_src} bf16_tflops (burst)",
+                         "traffic": NCU_TRAFFIC_BYTES},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": args.steps,
+            "launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
+                          "max": max(per_launch_ms)},
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=workloads.HEADLINE.name,
+                    choices=[x.name for x in workloads.WORKLOADS])
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="query rows per head timed for the CPU baseline")
+    ap.add_argument("--ref-rows", type=int, default=64,
+                    help="query rows per head per step of --impl reference")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = workloads.by_name(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
