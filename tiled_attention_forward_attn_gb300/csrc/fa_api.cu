@@ -38,9 +38,10 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
-template <int D>
+template <int D, bool kNeg>
 cudaError_t configure_kernel() {
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, kNeg>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::Cfg<D>::kSmemAlloc));
 }
 
@@ -61,7 +62,8 @@ int prepare_device(int* dev_out) {
     g_dev_state[dev] = -1;
     return FA_ERR_DEVICE;
   }
-  if (configure_kernel<64>() != cudaSuccess || configure_kernel<128>() != cudaSuccess)
+  if (configure_kernel<64, false>() != cudaSuccess || configure_kernel<64, true>() != cudaSuccess ||
+      configure_kernel<128, false>() != cudaSuccess || configure_kernel<128, true>() != cudaSuccess)
     return FA_ERR_LAUNCH;
   g_dev_state[dev] = 1;
   return FA_OK;
@@ -88,11 +90,13 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
-template <int D>
+template <int D, bool kNeg>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
            const CUtensorMap& mo, const fa::FwdParams& prm, int BH, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(prm.num_q_tiles));
-  fa::fa_fwd_kernel<D>
+  // x = batch*head, y = 256-row query unit (the kernel visits y in reverse,
+  // so the causal units with the most key tiles are dispatched first).
+  const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(prm.num_units));
+  fa::fa_fwd_kernel<D, kNeg>
       <<<grid, fa::kNumThreads, fa::Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, mo, prm);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -105,10 +109,10 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t num_q_tiles = (static_cast<int64_t>(N) + fa::kBlockM - 1) / fa::kBlockM;
-  // grid.x = B*H (<= 2^31-1), grid.y = query tiles (<= 65535); element
-  // offsets bh*N + row must fit in int for the LSE store.
-  if (BH > INT_MAX || num_q_tiles > 65535 || BH * N > INT_MAX) return FA_ERR_SHAPE;
+  const int64_t num_units = (static_cast<int64_t>(N) + fa::kUnitM - 1) / fa::kUnitM;
+  // grid.x = B*H (<= 2^31-1), grid.y = 256-row query units (<= 65535);
+  // element offsets bh*N + row must fit in int for the LSE store.
+  if (BH > INT_MAX || num_units > 65535 || BH * N > INT_MAX) return FA_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) &
       15u)
@@ -140,15 +144,25 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   fa::FwdParams prm;
   prm.lse = lse;
   prm.N = N;
-  prm.num_q_tiles = static_cast<int>(num_q_tiles);
+  prm.num_units = static_cast<int>(num_units);
   prm.causal = causal;
-  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // scale * log2(e).  A zero scale is passed as 1e-30: every scaled score is
+  // then below 1e-25 in magnitude, so 2^x rounds to exactly 1 in fp32 as for
+  // a true zero, while a masked score (-inf) still maps to -inf.
+  double c = static_cast<double>(scale) * 1.4426950408889634;
+  if (c == 0.0) c = 1e-30;
+  prm.scale_log2 = static_cast<float>(c);
   prm.inject = g_inject.load(std::memory_order_relaxed);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (d == 64) return launch<64>(mq, mk, mv, mo, prm, static_cast<int>(BH), s);
-  return launch<128>(mq, mk, mv, mo, prm, static_cast<int>(BH), s);
+  const bool neg = prm.scale_log2 < 0.0f;
+  const int bh = static_cast<int>(BH);
+  if (d == 64)
+    return neg ? launch<64, true>(mq, mk, mv, mo, prm, bh, s)
+               : launch<64, false>(mq, mk, mv, mo, prm, bh, s);
+  return neg ? launch<128, true>(mq, mk, mv, mo, prm, bh, s)
+             : launch<128, false>(mq, mk, mv, mo, prm, bh, s);
 }
 
 extern "C" const char* fa_strerror(int code) {
