@@ -38,8 +38,16 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
+// Sets the dynamic shared-memory size, and checks that the kernel was built
+// with exactly the per-thread register count its setmaxnreg split assumes
+// (a different count could leave the softmax warpgroups waiting for
+// registers that the pool does not hold).
 template <int D, bool kNeg>
 cudaError_t configure_kernel() {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, kNeg>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != static_cast<int>(fa::kLaunchRegs)) return cudaErrorInvalidKernelImage;
   return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, kNeg>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::Cfg<D>::kSmemAlloc));

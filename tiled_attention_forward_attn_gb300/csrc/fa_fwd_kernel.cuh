@@ -12,11 +12,19 @@
 //
 // One CTA = one (batch*head, 256-row query unit) = two 128-row query tiles,
 // "A" (rows q0..q0+127) and "B" (rows q0+128..q0+255), that share every K/V
-// tile loaded.  Ten warps:
-//   warps 0-3  softmax of tile A; thread t owns row t of A = TMEM lane t
-//   warps 4-7  softmax of tile B; thread t owns row t of B = TMEM lane t
-//   warp 8     TMA producer: Q_A, Q_B once, then K_j and V_j into SMEM rings
-//   warp 9     TMEM allocator and tcgen05.mma issuer
+// tile loaded.  Three warpgroups:
+//   warps 0-3   softmax of tile A; thread t owns row t of A = TMEM lane t
+//   warps 4-7   softmax of tile B; thread t owns row t of B = TMEM lane t
+//   warp 8      TMA producer of Q_A, Q_B (once) and the K_j ring
+//   warp 9      TMEM allocator and tcgen05.mma issuer
+//   warp 10     TMA producer of the V_j ring
+//   warp 11     idle (it completes the third warpgroup)
+// K and V have separate rings and producers, so neither ring's refill waits
+// behind the other's; the rings are as deep as shared memory allows because
+// a K/V tile copy takes a few microseconds to land under full load.
+// The third warpgroup hands most of its registers to the two softmax
+// warpgroups (setmaxnreg): 384 threads launch with 168 registers each
+// (64512 in all); afterwards 256 x 232 + 128 x 40 = 64512 are in use.
 // The tensor core alternates between the tiles: while the softmax warps of A
 // turn S_A(j) into P_A(j), it computes P_B(j-1) V_(j-1) and S_B(j), and vice
 // versa, so the exponentials of one tile overlap the MMAs of the other.
@@ -52,10 +60,17 @@ constexpr int kTileM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kTilesPerCta = 2;
 constexpr int kUnitM = kTileM * kTilesPerCta;  // query rows per CTA
 constexpr int kBlockN = 128;                   // keys per K/V tile
-constexpr int kNumThreads = 320;
+constexpr int kNumThreads = 384;
+constexpr uint32_t kLaunchRegs = 168;    // 65536 / (3 warps per sub-partition x 32 x 4)
+constexpr uint32_t kSoftmaxRegs = 232;   // after setmaxnreg.inc
+constexpr uint32_t kControlRegs = 40;    // after setmaxnreg.dec
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kNumThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+static_assert(2 * kSoftmaxRegs + kControlRegs <= 512, "per-sub-partition register file");
 constexpr int kRowThreadsPerTile = 128;
-constexpr int kLoadWarp = 8;
+constexpr int kLoadWarp = 8;    // Q and K producer
 constexpr int kMmaWarp = 9;
+constexpr int kLoadVWarp = 10;  // V producer
 constexpr uint32_t kSwBlockBytes = 128 * 128;  // [128 rows x 64 bf16] swizzled block
 constexpr float kRescaleThreshold = 8.0f;      // log2 units: P stays <= 2^8
 
@@ -77,19 +92,23 @@ struct FwdParams {
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension");
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  // Ring depths: 64 KB of Q plus 3 K and 2 V tiles of 32 KB fill 224 KB at
+  // D = 128; at D = 64 the tiles are half as large.
+  static constexpr int kStagesK = (D == 64) ? 4 : 3;
+  static constexpr int kStagesV = (D == 64) ? 4 : 2;
   static constexpr uint32_t kQBytes = kTileM * D * 2;  // one query tile
   static constexpr uint32_t kKVBytes = kBlockN * D * 2;
   static constexpr uint32_t kOffQ = 0;  // Q_A, Q_B
   static constexpr uint32_t kOffK = kOffQ + kTilesPerCta * kQBytes;
-  static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
+  static constexpr uint32_t kOffV = kOffK + kStagesK * kKVBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStagesV * kKVBytes;
   // q_full[2], s_full[2], p_full[2], o_done[2], mma_done,
-  // k_full[S], k_empty[S], v_full[S], v_empty[S]
-  static constexpr int kNumBars = 9 + 4 * kStages;
+  // k_full[SK], k_empty[SK], v_full[SV], v_empty[SV]
+  static constexpr int kNumBars = 9 + 2 * kStagesK + 2 * kStagesV;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kSmemAlloc <= 232448, "dynamic shared memory per block");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_t at kColS + 128*t, P_t over its first 64 columns
   static constexpr uint32_t kColO = 256;  // O_t at kColO + D*t
@@ -100,16 +119,16 @@ struct Cfg {
 // Barrier addresses (8 bytes each) in the order of the layout above.
 struct Barriers {
   uint32_t base;
-  int stages;
+  int sk, sv;  // K and V ring depths
   __device__ uint32_t q_full(int t) const { return base + 8u * t; }
   __device__ uint32_t s_full(int t) const { return base + 16u + 8u * t; }
   __device__ uint32_t p_full(int t) const { return base + 32u + 8u * t; }
   __device__ uint32_t o_done(int t) const { return base + 48u + 8u * t; }
   __device__ uint32_t mma_done() const { return base + 64u; }
   __device__ uint32_t k_full(int s) const { return base + 72u + 8u * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 72u + 8u * (stages + s); }
-  __device__ uint32_t v_full(int s) const { return base + 72u + 8u * (2 * stages + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 72u + 8u * (3 * stages + s); }
+  __device__ uint32_t k_empty(int s) const { return base + 72u + 8u * (sk + s); }
+  __device__ uint32_t v_full(int s) const { return base + 72u + 8u * (2 * sk + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 72u + 8u * (2 * sk + sv + s); }
 };
 
 struct WaitCtx {
@@ -124,7 +143,7 @@ __device__ __forceinline__ void record_timeout(const WaitCtx& w) {
 
 // Slow path of wait_bar: poll until the phase completes, the CTA aborts or
 // the time limit expires.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const WaitCtx& w) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -153,7 +172,7 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, con
 
 // Bounded wait used while draining: ignores the abort flag (copies and MMAs
 // already issued always complete), bounded by time alone.
-__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+__device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const WaitCtx& w) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -175,19 +194,6 @@ __device__ __forceinline__ bool tile_threads_all(uint32_t id, bool v) {
       : "r"(id), "r"(static_cast<uint32_t>(v))
       : "memory");
   return r != 0;
-}
-
-// Descriptor of the 16-wide K slice `kk` of a K-major operand stored as
-// [rows x 64] swizzled blocks (block b holds K columns [64b, 64b+64)).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
-  return smem_desc_sw128(base + (kk >> 2) * kSwBlockBytes + (kk & 3) * 32, 16, 1024);
-}
-
-// Descriptor of the 16-row K slice `kk` of the MN-major V tile: rows are keys
-// (the K dimension), 128-byte rows hold 64 head-dim columns; the next 64
-// columns sit one swizzled block further (leading-dimension offset).
-__device__ __forceinline__ uint64_t v_desc(uint32_t base, int kk) {
-  return smem_desc_sw128(base + kk * 16 * 128, kSwBlockBytes, 1024);
 }
 
 // Byte offset of the 16-byte chunk `chunk` (0..D/8-1) of row `row` in a
@@ -331,7 +337,8 @@ __device__ __forceinline__ void softmax_tile(const int t, const int n_tiles, con
     }
     tmem_st_wait();
     tc_fence_before_sync();
-    mbar_arrive(bars.p_full(t));
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bars.p_full(t));
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -379,7 +386,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
   using C = Cfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kStagesK;
+  constexpr int SV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t sV = sbase + C::kOffV;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
-  const Barriers bars{sbase + C::kOffBar, S};
+  const Barriers bars{sbase + C::kOffBar, SK, SV};
   const WaitCtx wctx{abort_flag, p.wait_limit_ns};
 
   const int warp = threadIdx.x >> 5;
@@ -406,13 +414,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int t = 0; t < kTilesPerCta; ++t) {
       mbar_init(bars.q_full(t), 1);
       mbar_init(bars.s_full(t), 1);
-      mbar_init(bars.p_full(t), kRowThreadsPerTile);
+      mbar_init(bars.p_full(t), kRowThreadsPerTile / 32);  // one arrival per warp
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.mma_done(), 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(bars.k_full(s), 1);
       mbar_init(bars.k_empty(s), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(bars.v_full(s), 1);
       mbar_init(bars.v_empty(s), 1);
     }
@@ -436,19 +446,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp < kLoadWarp) {
     // ------------------------------------------------------------ softmax
+    setmaxnreg_inc<kSoftmaxRegs>();
     const int t = warp >> 2;
     softmax_tile<D, kNegScale>(t, n_t[t], q0 + kTileM * t, tmem, sQ + t * C::kQBytes, bars, wctx,
                                &tm_o, p, bh);
   } else if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ Q, K producer
+    setmaxnreg_dec<kControlRegs>();
     if (lane == 0) {
-      int k_issued = 0, v_issued = 0;  // K_j / V_j copies issued for j < *_issued
-      bool v0_skipped = false;
+      int issued = 0;  // K_j copies issued for j < issued
       bool q_issued[kTilesPerCta] = {false, false};
       for (int j = 0; j < n_max; ++j) {
-        const int s = j % S;
-        const uint32_t ph = static_cast<uint32_t>(j / S) & 1u;
-        if (j >= S && !wait_bar(bars.k_empty(s), ph ^ 1u, wctx)) break;
+        const int s = j % SK;
+        if (j >= SK && !wait_bar(bars.k_empty(s), (static_cast<uint32_t>(j / SK) & 1u) ^ 1u, wctx))
+          break;
         if (j == 0) {  // Q_A first: S_A(0) needs only Q_A and K_0
           mbar_arrive_expect_tx(bars.q_full(0), C::kQBytes);
 #pragma unroll
@@ -461,7 +472,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int b = 0; b < D / 64; ++b)
           tma_load_3d(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s), 64 * b,
                       j * kBlockN, bh);
-        k_issued = j + 1;
+        issued = j + 1;
         if (j == 0 && n_t[1] > 0) {
           mbar_arrive_expect_tx(bars.q_full(1), C::kQBytes);
 #pragma unroll
@@ -470,8 +481,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         q0 + kTileM, bh);
           q_issued[1] = true;
         }
-        if (j >= S && !wait_bar(bars.v_empty(s), ph ^ 1u, wctx)) break;
-        v_issued = j + 1;
+      }
+      // Drain: every copy issued must land before the CTA may exit.  The last
+      // copy into stage s is the largest j < issued with j % SK == s.
+#pragma unroll
+      for (int t = 0; t < kTilesPerCta; ++t)
+        if (q_issued[t]) wait_bar_drain(bars.q_full(t), 0, wctx);
+#pragma unroll
+      for (int s = 0; s < SK; ++s) {
+        if (issued > s) {
+          const int jl = issued - 1 - ((issued - 1 - s) % SK);
+          wait_bar_drain(bars.k_full(s), static_cast<uint32_t>(jl / SK) & 1u, wctx);
+        }
+      }
+    }
+  } else if (warp == kLoadVWarp) {
+    // ------------------------------------------------------------ V producer
+    setmaxnreg_dec<kControlRegs>();
+    if (lane == 0) {
+      int issued = 0;  // V_j copies issued (or deliberately skipped) for j < issued
+      bool v0_skipped = false;
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % SV;
+        if (j >= SV && !wait_bar(bars.v_empty(s), (static_cast<uint32_t>(j / SV) & 1u) ^ 1u, wctx))
+          break;
+        issued = j + 1;
         if (j == 0 && (p.inject & kInjectSkipFirstV)) {
           v0_skipped = true;
           continue;
@@ -482,48 +516,53 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           tma_load_3d(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s), 64 * b,
                       j * kBlockN, bh);
       }
-      // Drain: every copy issued must land before the CTA may exit.  The last
-      // copy into stage s is the largest j < *_issued with j % S == s.
 #pragma unroll
-      for (int t = 0; t < kTilesPerCta; ++t)
-        if (q_issued[t]) wait_bar_drain(bars.q_full(t), 0, wctx);
-#pragma unroll
-      for (int s = 0; s < S; ++s) {
-        if (k_issued > s) {
-          const int jl = k_issued - 1 - ((k_issued - 1 - s) % S);
-          wait_bar_drain(bars.k_full(s), static_cast<uint32_t>(jl / S) & 1u, wctx);
-        }
-        if (v_issued > s) {
-          const int jl = v_issued - 1 - ((v_issued - 1 - s) % S);
+      for (int s = 0; s < SV; ++s) {
+        if (issued > s) {
+          const int jl = issued - 1 - ((issued - 1 - s) % SV);
           if (!(jl == 0 && v0_skipped))
-            wait_bar_drain(bars.v_full(s), static_cast<uint32_t>(jl / S) & 1u, wctx);
+            wait_bar_drain(bars.v_full(s), static_cast<uint32_t>(jl / SV) & 1u, wctx);
         }
       }
     }
-  } else {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<kControlRegs>();
     if (lane == 0) {
+      // Descriptor halves.  Every operand sits at a fixed SMEM address, so
+      // the low halves of all descriptors are a base plus compile-time
+      // offsets (>> 4) and each MMA issue costs a couple of integer adds.
+      constexpr uint32_t kHi = desc_hi_sw128(1024);
+      const uint32_t q_lo = desc_lo(sQ, 16);
+      const uint32_t k_lo = desc_lo(sK, 16);
+      const uint32_t v_lo = desc_lo(sV, kSwBlockBytes);
+      // K-major slice kk of a [128 x D] tile: block kk/4, 32 bytes per slice.
+      auto kmaj_off = [](int kk) -> uint32_t {
+        return ((kk >> 2) * kSwBlockBytes + (kk & 3) * 32) >> 4;
+      };
       auto issue_s = [&](int t, int j) {
-        const uint32_t kbase = sK + (j % S) * C::kKVBytes;
-        const uint32_t qbase = sQ + t * C::kQBytes;
+        const uint32_t a_lo = q_lo + ((t * C::kQBytes) >> 4);
+        const uint32_t b_lo = k_lo + (((j % SK) * C::kKVBytes) >> 4);
         const uint32_t d_tmem = tmem + C::kColS + 128u * t;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(d_tmem, kmajor_desc(qbase, kk), kmajor_desc(kbase, kk), C::kIdescQK,
-                  kk > 0 ? 1u : 0u);
+          umma_ss_lohi(d_tmem, a_lo + kmaj_off(kk), kHi, b_lo + kmaj_off(kk), kHi, C::kIdescQK,
+                       kk > 0 ? 1u : 0u);
         umma_commit(bars.s_full(t));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t vbase = sV + (j % S) * C::kKVBytes;
+        // V slice kk: 16 key rows of 128 bytes.
+        const uint32_t b_lo = v_lo + (((j % SV) * C::kKVBytes) >> 4);
         const uint32_t p_tmem = tmem + C::kColS + 128u * t;
         const uint32_t d_tmem = tmem + C::kColO + static_cast<uint32_t>(D) * t;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_ts(d_tmem, p_tmem + 8u * kk, v_desc(vbase, kk), C::kIdescPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_lohi(d_tmem, p_tmem + 8u * kk, b_lo + ((kk * 16 * 128) >> 4), kHi, C::kIdescPV,
+                       kk > 0 ? 1u : acc0);
       };
       auto wait_k = [&](int j) {
-        return wait_bar(bars.k_full(j % S), static_cast<uint32_t>(j / S) & 1u, wctx);
+        return wait_bar(bars.k_full(j % SK), static_cast<uint32_t>(j / SK) & 1u, wctx);
       };
 
       bool ok = wait_k(0) && wait_bar(bars.q_full(0), 0, wctx);
@@ -539,10 +578,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         if (ok) umma_commit(bars.k_empty(0));
       }
+      // Issuing a tcgen05.mma waits for room in the tensor core's queue, so
+      // this thread runs only a little ahead of the MMAs: every wait, fence
+      // or commit between two MMA groups is tensor-core idle time.  All
+      // waits of an iteration therefore come first (the TMA waits are
+      // normally already satisfied), and commits are batched after groups.
       for (int j = 0; ok && j < n_max; ++j) {
-        const int s = j % S;
-        if (!wait_bar(bars.v_full(s), static_cast<uint32_t>(j / S) & 1u, wctx)) break;
-        bool k_next_ready = false;
+        const int s = j % SV;
+        const bool more = j + 1 < n_max;
+        if (!wait_bar(bars.v_full(s), static_cast<uint32_t>(j / SV) & 1u, wctx)) break;
+        if (more && !wait_k(j + 1)) break;
 #pragma unroll
         for (int t = 0; t < kTilesPerCta; ++t) {
           if (j >= n_t[t]) continue;
@@ -552,27 +597,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           tc_fence_after_sync();
           issue_pv(t, j);
-          if (j + 1 == n_t[t]) umma_commit(bars.o_done(t));
-          // V_j is free once the last tile that uses it has consumed it.
-          if (t == kTilesPerCta - 1 || j >= n_t[kTilesPerCta - 1]) umma_commit(bars.v_empty(s));
           if (j + 1 < n_t[t]) {
-            if (!k_next_ready) {
-              if (!wait_k(j + 1)) {
-                ok = false;
-                break;
-              }
-              k_next_ready = true;
-              tc_fence_after_sync();
-            }
-            issue_s(t, j + 1);
+            issue_s(t, j + 1);  // commits s_full(t), which also covers P_t(j) V_j
+          } else {
+            umma_commit(bars.o_done(t));
           }
         }
-        if (ok && k_next_ready) umma_commit(bars.k_empty((j + 1) % S));
+        if (!ok) break;
+        umma_commit(bars.v_empty(s));                 // V_j: both P.V products issued
+        if (more) umma_commit(bars.k_empty((j + 1) % SK));  // K_j+1: both S MMAs issued
       }
       // Drain: wait for every MMA issued by this thread.
       umma_commit(bars.mma_done());
       wait_bar_drain(bars.mma_done(), 0, wctx);
     }
+  } else {
+    setmaxnreg_dec<kControlRegs>();  // idle warp 11
   }
 
   // ------------------------------------------------------------ teardown

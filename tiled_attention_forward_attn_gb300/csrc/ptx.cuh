@@ -23,16 +23,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool elect_one_sync() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
@@ -111,11 +101,6 @@ __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Wait until every committed bulk store has finished reading shared memory.
-__device__ __forceinline__ void tma_store_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -141,6 +126,19 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// Per-warpgroup register reallocation (all four warps of the warpgroup
+// execute it).  `dec` releases registers to the CTA's pool; `inc` waits until
+// the pool can supply the requested count.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 __device__ __forceinline__ void tc_fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -152,28 +150,6 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 // ----------------------------------------------------------------------------
 // tcgen05: MMA
 // ----------------------------------------------------------------------------
-// D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f16 (bf16 in, fp32 acc).
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -182,21 +158,52 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle.
+// Shared-memory matrix descriptors (64 bits, 128-byte swizzle):
 //   bits  0-13 start address >> 4
 //   bits 16-29 leading-dimension byte offset >> 4
 //   bits 32-45 stride-dimension byte offset >> 4
 //   bits 46-48 fixed 0b001
 //   bits 61-63 swizzle mode (2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
-  uint64_t desc = 0;
-  desc |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  desc |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  desc |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  desc |= static_cast<uint64_t>(1) << 46;
-  desc |= static_cast<uint64_t>(2) << 61;
-  return desc;
+// The MMA wrappers below take each descriptor as its two 32-bit halves (lo:
+// start address and leading offset; hi: stride offset, version, swizzle), so
+// callers can step through K slices with a single 32-bit add on the low half.
+//
+// D[tmem] (+)= A[smem] * B[smem]; kind::f16 (bf16 in, fp32 accumulate).
+__device__ __forceinline__ void umma_ss_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                             uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], B descriptor as two halves.
+__device__ __forceinline__ void umma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Low half of a 128-byte-swizzle descriptor: start address >> 4 (bits 0-13)
+// and leading-dimension byte offset >> 4 (bits 16-29).
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+
+// High half: stride-dimension byte offset >> 4 (bits 32-45), the fixed
+// 0b001 at bits 46-48, swizzle mode 2 (128-byte) at bits 61-63.
+__host__ __device__ constexpr uint32_t desc_hi_sw128(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and an fp32 accumulator.
