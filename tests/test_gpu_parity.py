@@ -48,9 +48,10 @@ def test_ragged(dev, N, d, causal):
     check_against_oracle(q, k, v, causal, 1.0 / math.sqrt(d), dev, label=f"ragged N{N} d{d} c{causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("scale", [0.0, -0.2, 0.9])
-def test_unusual_scales(dev, scale):
-    q, k, v = workloads.generate_shape(2, 1, 300, 64, seed=300)
+def test_unusual_scales(dev, scale, d):
+    q, k, v = workloads.generate_shape(2, 1, 300, d, seed=300)
     check_against_oracle(q, k, v, True, scale, dev, label=f"scale {scale}")
     check_against_oracle(q, k, v, False, scale, dev, label=f"scale {scale}")
 

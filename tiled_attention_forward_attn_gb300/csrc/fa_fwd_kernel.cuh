@@ -444,15 +444,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Register reallocation: one setmaxnreg per warpgroup, executed by all
+  // four of its warps at the same instruction (it is warpgroup-aligned).
+  if (warp < kLoadWarp) {
+    setmaxnreg_inc<kSoftmaxRegs>();
+  } else {
+    setmaxnreg_dec<kControlRegs>();
+  }
+
   if (warp < kLoadWarp) {
     // ------------------------------------------------------------ softmax
-    setmaxnreg_inc<kSoftmaxRegs>();
     const int t = warp >> 2;
     softmax_tile<D, kNegScale>(t, n_t[t], q0 + kTileM * t, tmem, sQ + t * C::kQBytes, bars, wctx,
                                &tm_o, p, bh);
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------------------ Q, K producer
-    setmaxnreg_dec<kControlRegs>();
     if (lane == 0) {
       int issued = 0;  // K_j copies issued for j < issued
       bool q_issued[kTilesPerCta] = {false, false};
@@ -497,7 +503,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp == kLoadVWarp) {
     // ------------------------------------------------------------ V producer
-    setmaxnreg_dec<kControlRegs>();
     if (lane == 0) {
       int issued = 0;  // V_j copies issued (or deliberately skipped) for j < issued
       bool v0_skipped = false;
@@ -527,7 +532,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    setmaxnreg_dec<kControlRegs>();
     if (lane == 0) {
       // Descriptor halves.  Every operand sits at a fixed SMEM address, so
       // the low halves of all descriptors are a base plus compile-time
@@ -611,8 +615,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       umma_commit(bars.mma_done());
       wait_bar_drain(bars.mma_done(), 0, wctx);
     }
-  } else {
-    setmaxnreg_dec<kControlRegs>();  // idle warp 11
   }
 
   // ------------------------------------------------------------ teardown
