@@ -28,6 +28,7 @@ cudaError_t g_encode_err = cudaSuccess;
 // Per-device readiness: 0 = unchecked, 1 = supported and configured, -1 = unsupported.
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices] = {0};
+int g_dev_sms[kMaxDevices] = {0};  // multiprocessor count of each configured device
 
 void load_encode() {
   cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -54,13 +55,16 @@ cudaError_t configure_kernel() {
 }
 
 // Checks that the current device is sm_103 and configures the kernels for it once.
-int prepare_device(int* dev_out) {
+int prepare_device(int* dev_out, int* sms_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
   *dev_out = dev;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
-  if (g_dev_state[dev] == 1) return FA_OK;
+  if (g_dev_state[dev] == 1) {
+    *sms_out = g_dev_sms[dev];
+    return FA_OK;
+  }
   if (g_dev_state[dev] == -1) return FA_ERR_DEVICE;
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -70,9 +74,14 @@ int prepare_device(int* dev_out) {
     g_dev_state[dev] = -1;
     return FA_ERR_DEVICE;
   }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return FA_ERR_LAUNCH;
   if (configure_kernel<64, false>() != cudaSuccess || configure_kernel<64, true>() != cudaSuccess ||
       configure_kernel<128, false>() != cudaSuccess || configure_kernel<128, true>() != cudaSuccess)
     return FA_ERR_LAUNCH;
+  g_dev_sms[dev] = sms;
+  *sms_out = sms;
   g_dev_state[dev] = 1;
   return FA_OK;
 }
@@ -98,14 +107,14 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
+// Persistent launch: one CTA per multiprocessor (at most one per work unit);
+// each CTA walks its share of the units inside the kernel.
 template <int D, bool kNeg>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-           const CUtensorMap& mo, const fa::FwdParams& prm, int BH, cudaStream_t stream) {
-  // x = batch*head, y = 256-row query unit (the kernel visits y in reverse,
-  // so the causal units with the most key tiles are dispatched first).
-  const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(prm.num_units));
-  fa::fa_fwd_kernel<D, kNeg>
-      <<<grid, fa::kNumThreads, fa::Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, mo, prm);
+           const fa::FwdParams& prm, int sms, cudaStream_t stream) {
+  const unsigned ctas = static_cast<unsigned>(prm.total_units < sms ? prm.total_units : sms);
+  fa::fa_fwd_kernel<D, kNeg><<<ctas, fa::kNumThreads, fa::Cfg<D>::kSmemAlloc, stream>>>(
+      mq, mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -118,9 +127,9 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
   const int64_t BH = static_cast<int64_t>(B) * H;
   const int64_t num_units = (static_cast<int64_t>(N) + fa::kUnitM - 1) / fa::kUnitM;
-  // grid.x = B*H (<= 2^31-1), grid.y = 256-row query units (<= 65535);
-  // element offsets bh*N + row must fit in int for the LSE store.
-  if (BH > INT_MAX || num_units > 65535 || BH * N > INT_MAX) return FA_ERR_SHAPE;
+  // Work units (B*H x 256-row query units) are counted in int, and so are
+  // the row offsets bh*N + row of the LSE store.
+  if (BH > INT_MAX || BH * num_units > INT_MAX || BH * N > INT_MAX) return FA_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) &
       15u)
@@ -136,23 +145,25 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   }
   if (overlaps(o, tensor_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
 
-  int dev = 0;
-  const int prep = prepare_device(&dev);
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
   if (prep != FA_OK) return prep;
   std::call_once(g_encode_once, load_encode);
   if (g_encode == nullptr) return FA_ERR_LAUNCH;
 
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv;
   if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
       !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
-      !encode_map(&mv, v, static_cast<int>(BH), N, d) ||
-      !encode_map(&mo, o, static_cast<int>(BH), N, d))
+      !encode_map(&mv, v, static_cast<int>(BH), N, d))
     return FA_ERR_LAUNCH;
 
   fa::FwdParams prm;
+  prm.o = static_cast<uint16_t*>(o);
   prm.lse = lse;
   prm.N = N;
+  prm.num_bh = static_cast<int>(BH);
   prm.num_units = static_cast<int>(num_units);
+  prm.total_units = static_cast<int>(BH * num_units);
   prm.causal = causal;
   // scale * log2(e).  A zero scale is passed as 1e-30: every scaled score is
   // then below 1e-25 in magnitude, so 2^x rounds to exactly 1 in fp32 as for
@@ -165,12 +176,9 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool neg = prm.scale_log2 < 0.0f;
-  const int bh = static_cast<int>(BH);
   if (d == 64)
-    return neg ? launch<64, true>(mq, mk, mv, mo, prm, bh, s)
-               : launch<64, false>(mq, mk, mv, mo, prm, bh, s);
-  return neg ? launch<128, true>(mq, mk, mv, mo, prm, bh, s)
-             : launch<128, false>(mq, mk, mv, mo, prm, bh, s);
+    return neg ? launch<64, true>(mq, mk, mv, prm, sms, s) : launch<64, false>(mq, mk, mv, prm, sms, s);
+  return neg ? launch<128, true>(mq, mk, mv, prm, sms, s) : launch<128, false>(mq, mk, mv, prm, sms, s);
 }
 
 extern "C" const char* fa_strerror(int code) {

@@ -4,27 +4,28 @@
 // Method: the tiled online softmax of "Parsing FlashAttention (2):
 // FlashAttention-v1 forward pass" (§2-§3: running max m, running exponent sum
 // l, accumulator rescaled by exp(m_old - m_new) when the max grows) in the
-// loop order of "Online Softmax and FlashAttention" (course unit 12: one CTA
-// keeps its Q tiles and output accumulators on chip for the whole K/V sweep;
+// loop order of "Online Softmax and FlashAttention" (course unit 12: query
+// tiles and their output accumulators stay on chip for the whole K/V sweep;
 // fully-future tiles are never loaded; diagonal tiles are masked element by
 // element; the unnormalised accumulator is divided by l once at the end).
 // No score or probability tile ever leaves the SM.
 //
-// One CTA = one (batch*head, 256-row query unit) = two 128-row query tiles,
+// Work unit = one (batch*head, 256-row query unit) = two 128-row query tiles,
 // "A" (rows q0..q0+127) and "B" (rows q0+128..q0+255), that share every K/V
-// tile loaded.  Three warpgroups:
-//   warps 0-3   softmax of tile A; thread t owns row t of A = TMEM lane t
-//   warps 4-7   softmax of tile B; thread t owns row t of B = TMEM lane t
-//   warp 8      TMA producer of Q_A, Q_B (once) and the K_j ring
-//   warp 9      TMEM allocator and tcgen05.mma issuer
+// tile loaded.  The grid is persistent: one CTA per SM walks the units in a
+// fixed order, heaviest (most key tiles) first, dealt to the CTAs in a
+// serpentine so per-CTA totals stay balanced; the next unit's Q and K/V
+// tiles stream in while the current unit finishes.  Three warpgroups:
+//   warps 0-3   softmax and epilogue of tile A; thread t owns row t = TMEM lane t
+//   warps 4-7   softmax and epilogue of tile B
+//   warp 8      TMA producer of Q_A, Q_B and the K_j ring
+//   warp 9      TMEM allocator and the tcgen05.mma issuer
 //   warp 10     TMA producer of the V_j ring
 //   warp 11     idle (it completes the third warpgroup)
-// K and V have separate rings and producers, so neither ring's refill waits
-// behind the other's; the rings are as deep as shared memory allows because
-// a K/V tile copy takes a few microseconds to land under full load.
 // The third warpgroup hands most of its registers to the two softmax
 // warpgroups (setmaxnreg): 384 threads launch with 168 registers each
-// (64512 in all); afterwards 256 x 232 + 128 x 40 = 64512 are in use.
+// (64512 in all); afterwards 256 x 216 + 128 x 72 = 64512 are in use.
+//
 // The tensor core alternates between the tiles: while the softmax warps of A
 // turn S_A(j) into P_A(j), it computes P_B(j-1) V_(j-1) and S_B(j), and vice
 // versa, so the exponentials of one tile overlap the MMAs of the other.
@@ -35,7 +36,9 @@
 // from TMEM; the next S_t MMA is issued after that P.V MMA, and tcgen05.mma
 // operations of one thread execute in issue order.  Because the S_t(j) MMA is
 // also committed after P_t(j-1) V_(j-1), the softmax warps know O_t is
-// complete whenever S_t(j) is, and may rescale it in place.
+// complete whenever S_t(j) is, and may rescale it in place.  The first P.V
+// of the next unit overwrites O_t only after the softmax warps, which read
+// O_t in their epilogue, have handed over that unit's first P_t.
 //
 // Rescaling is lazy: the exponent reference m_ref of a row only moves when a
 // tile's maximum exceeds it by more than 8 (base-2 exponent units), so P, l
@@ -58,12 +61,12 @@ namespace fa {
 
 constexpr int kTileM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kTilesPerCta = 2;
-constexpr int kUnitM = kTileM * kTilesPerCta;  // query rows per CTA
+constexpr int kUnitM = kTileM * kTilesPerCta;  // query rows per work unit
 constexpr int kBlockN = 128;                   // keys per K/V tile
 constexpr int kNumThreads = 384;
-constexpr uint32_t kLaunchRegs = 168;    // 65536 / (3 warps per sub-partition x 32 x 4)
-constexpr uint32_t kSoftmaxRegs = 232;   // after setmaxnreg.inc
-constexpr uint32_t kControlRegs = 40;    // after setmaxnreg.dec
+constexpr uint32_t kLaunchRegs = 168;   // 65536 / (3 warps per sub-partition x 32 x 4)
+constexpr uint32_t kSoftmaxRegs = 216;  // after setmaxnreg.inc
+constexpr uint32_t kControlRegs = 72;   // after setmaxnreg.dec
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kNumThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 static_assert(2 * kSoftmaxRegs + kControlRegs <= 512, "per-sub-partition register file");
@@ -80,9 +83,12 @@ constexpr uint32_t kInjectSkipFirstV = 1u;  // test hook: never issue the first 
 __device__ uint32_t g_fa_status;
 
 struct FwdParams {
+  uint16_t* o;       // [BH][N][D] bf16 bit patterns
   float* lse;        // [BH][N] fp32
   int N;             // sequence length
-  int num_units;     // ceil(N / kUnitM)
+  int num_bh;        // B * H
+  int num_units;     // ceil(N / kUnitM) query units per (batch, head)
+  int total_units;   // num_bh * num_units
   int causal;        // 0 / 1
   float scale_log2;  // scale * log2(e); never 0 (scale 0 arrives as a tiny positive value)
   uint32_t inject;   // test hooks (0 in normal use)
@@ -102,9 +108,9 @@ struct Cfg {
   static constexpr uint32_t kOffK = kOffQ + kTilesPerCta * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStagesK * kKVBytes;
   static constexpr uint32_t kOffBar = kOffV + kStagesV * kKVBytes;
-  // q_full[2], s_full[2], p_full[2], o_done[2], mma_done,
+  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done,
   // k_full[SK], k_empty[SK], v_full[SV], v_empty[SV]
-  static constexpr int kNumBars = 9 + 2 * kStagesK + 2 * kStagesV;
+  static constexpr int kNumBars = 11 + 2 * kStagesK + 2 * kStagesV;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -121,14 +127,15 @@ struct Barriers {
   uint32_t base;
   int sk, sv;  // K and V ring depths
   __device__ uint32_t q_full(int t) const { return base + 8u * t; }
-  __device__ uint32_t s_full(int t) const { return base + 16u + 8u * t; }
-  __device__ uint32_t p_full(int t) const { return base + 32u + 8u * t; }
-  __device__ uint32_t o_done(int t) const { return base + 48u + 8u * t; }
-  __device__ uint32_t mma_done() const { return base + 64u; }
-  __device__ uint32_t k_full(int s) const { return base + 72u + 8u * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 72u + 8u * (sk + s); }
-  __device__ uint32_t v_full(int s) const { return base + 72u + 8u * (2 * sk + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 72u + 8u * (2 * sk + sv + s); }
+  __device__ uint32_t q_empty(int t) const { return base + 16u + 8u * t; }
+  __device__ uint32_t s_full(int t) const { return base + 32u + 8u * t; }
+  __device__ uint32_t p_full(int t) const { return base + 48u + 8u * t; }
+  __device__ uint32_t o_done(int t) const { return base + 64u + 8u * t; }
+  __device__ uint32_t mma_done() const { return base + 80u; }
+  __device__ uint32_t k_full(int s) const { return base + 88u + 8u * s; }
+  __device__ uint32_t k_empty(int s) const { return base + 88u + 8u * (sk + s); }
+  __device__ uint32_t v_full(int s) const { return base + 88u + 8u * (2 * sk + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 88u + 8u * (2 * sk + sv + s); }
 };
 
 struct WaitCtx {
@@ -182,25 +189,17 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
   return false;
 }
 
-// AND-reduce a flag over the 128 threads of one tile (named barrier `id`).
-__device__ __forceinline__ bool tile_threads_all(uint32_t id, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %2, 0;\n\t"
-      "bar.red.and.pred q, %1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(id), "r"(static_cast<uint32_t>(v))
-      : "memory");
-  return r != 0;
-}
+// Parity of the n-th completed phase (n = 0, 1, 2, ...) of a barrier.
+__device__ __forceinline__ uint32_t parity_of(uint32_t n) { return n & 1u; }
 
-// Byte offset of the 16-byte chunk `chunk` (0..D/8-1) of row `row` in a
-// [128 x D] tile stored as 128-byte-swizzled [128 x 64] blocks.
-__device__ __forceinline__ uint32_t swizzled_chunk(int row, int chunk) {
-  return (chunk >> 3) * kSwBlockBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
-}
+// ----------------------------------------------------------------------------
+// Work units
+// ----------------------------------------------------------------------------
+struct Unit {
+  int bh;    // batch * heads + head
+  int q0;    // first query row of tile A
+  int n[2];  // key tiles visited by tiles A and B (0 = tile past the end)
+};
 
 // Number of key tiles a query tile starting at row r0 must visit (0 when the
 // tile lies entirely past the end of the sequence).  Causal: key tiles whose
@@ -212,15 +211,38 @@ __device__ __forceinline__ int key_tiles_for(int r0, int N, int causal) {
   return (kv_end + kBlockN - 1) / kBlockN;
 }
 
+// The idx-th unit of the global order: query units from the last (most key
+// tiles under the causal mask) to the first, all heads of one query unit
+// together.
+__device__ __forceinline__ Unit unit_at(int idx, const FwdParams& p) {
+  Unit u;
+  const int qu = p.num_units - 1 - idx / p.num_bh;
+  u.bh = idx % p.num_bh;
+  u.q0 = qu * kUnitM;
+  u.n[0] = key_tiles_for(u.q0, p.N, p.causal);
+  u.n[1] = key_tiles_for(u.q0 + kTileM, p.N, p.causal);
+  return u;
+}
+
+// Index of this CTA's r-th unit: rounds of gridDim.x units, dealt left to
+// right in even rounds and right to left in odd ones (longest-first with a
+// serpentine keeps the per-CTA sums of decreasing costs even).  A value
+// >= total_units means the CTA has no r-th unit (nor any later one).
+__device__ __forceinline__ int unit_index(int r) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 // ----------------------------------------------------------------------------
-// Softmax warps of one query tile (128 threads, one row each)
+// Softmax warps: one query tile of one unit (128 threads, one row each)
 // ----------------------------------------------------------------------------
 template <int D, bool kNegScale>
-__device__ __forceinline__ void softmax_tile(const int t, const int n_tiles, const int r0,
-                                             const uint32_t tmem, const uint32_t sQt,
+__device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, const int r0,
+                                             const int bh, const uint32_t tmem,
                                              const Barriers& bars, const WaitCtx& wctx,
-                                             const CUtensorMap* tm_o, const FwdParams& p,
-                                             const int bh) {
+                                             const FwdParams& p, uint32_t& s_uses,
+                                             uint32_t& o_uses) {
   using C = Cfg<D>;
   const int row = threadIdx.x & 127;  // row within the tile = TMEM lane
   const int warp_in_tile = (threadIdx.x >> 5) & 3;
@@ -233,19 +255,19 @@ __device__ __forceinline__ void softmax_tile(const int t, const int n_tiles, con
   const int row_last_key = p.causal ? min(q_idx, p.N - 1) : p.N - 1;
   float m_ref = -CUDART_INF_F;  // exponent reference, scaled log2 units
   float l_run = 0.0f;           // sum of 2^(scaled score - m_ref)
-  bool ok = true;
 
   for (int j = 0; j < n_tiles; ++j) {
-    if (!warp_wait_bar(bars.s_full(t), static_cast<uint32_t>(j) & 1u, wctx)) {
-      ok = false;
-      break;
-    }
+    if (!warp_wait_bar(bars.s_full(t), parity_of(s_uses), wctx)) return false;
+    ++s_uses;
     tc_fence_after_sync();
     uint32_t sr[kBlockN];
 #pragma unroll
     for (int cc = 0; cc < kBlockN / 32; ++cc)
       tmem_ld32(s_addr + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * cc]));
     tmem_ld_wait();
+#pragma unroll
+    for (int cc = 0; cc < kBlockN / 32; ++cc)
+      tmem_ld_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * cc]));
     float s[kBlockN];
 #pragma unroll
     for (int i = 0; i < kBlockN; ++i) s[i] = __uint_as_float(sr[i]);
@@ -325,6 +347,7 @@ __device__ __forceinline__ void softmax_tile(const int t, const int n_tiles, con
         uint32_t o[32];
         tmem_ld32(o_addr + 32 * cc, o);
         tmem_ld_wait();
+        tmem_ld_fence(o);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float a0, a1;
@@ -342,49 +365,42 @@ __device__ __forceinline__ void softmax_tile(const int t, const int n_tiles, con
   }
 
   // ---------------------------------------------------------------- epilogue
-  if (ok && n_tiles > 0 && !warp_wait_bar(bars.o_done(t), 0u, wctx)) ok = false;
-  if (tile_threads_all(1u + t, ok) && n_tiles > 0) {
-    tc_fence_after_sync();
-    const float inv_l = 1.0f / l_run;
-    // Q_t is dead (its last MMA completed before the last P.V), so its SMEM
-    // stages the bf16 output for the TMA store.
+  // O = O_t / l as bf16, straight from registers to global memory (each
+  // thread writes its own row, 2*D contiguous bytes), then LSE.
+  if (!warp_wait_bar(bars.o_done(t), parity_of(o_uses), wctx)) return false;
+  ++o_uses;
+  tc_fence_after_sync();
+  const float inv_l = 1.0f / l_run;
+  const bool in_range = q_idx < p.N;
+  uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.N + q_idx) * D);
 #pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
-      uint32_t o[32];
-      tmem_ld32(o_addr + 32 * cc, o);
-      tmem_ld_wait();
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t o[32];
+    tmem_ld32(o_addr + 32 * cc, o);
+    tmem_ld_wait();
+    tmem_ld_fence(o);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t w4[4];
+    for (int g = 0; g < 4; ++g) {
+      uint32_t w4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float a0, a1;
-          fmul2(a0, a1, __uint_as_float(o[8 * g + 2 * e]), __uint_as_float(o[8 * g + 2 * e + 1]),
-                inv_l, inv_l);
-          w4[e] = pack_bf16x2(a0, a1);
-        }
-        st_shared_v4(sQt + swizzled_chunk(row, 4 * cc + g), w4[0], w4[1], w4[2], w4[3]);
+      for (int e = 0; e < 4; ++e) {
+        float a0, a1;
+        fmul2(a0, a1, __uint_as_float(o[8 * g + 2 * e]), __uint_as_float(o[8 * g + 2 * e + 1]),
+              inv_l, inv_l);
+        w4[e] = pack_bf16x2(a0, a1);
       }
+      if (in_range) dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
     }
-    fence_proxy_async_smem();
-    named_barrier_sync(1u + t, kRowThreadsPerTile);
-    if (row == 0) {
-#pragma unroll
-      for (int b = 0; b < D / 64; ++b) tma_store_3d(tm_o, sQt + b * kSwBlockBytes, 64 * b, r0, bh);
-      tma_store_commit();
-      tma_store_wait_all();
-    }
-    if (q_idx < p.N)
-      p.lse[static_cast<size_t>(bh) * p.N + q_idx] =
-          (m_ref + __log2f(l_run)) * 0.6931471805599453f;
   }
+  if (in_range)
+    p.lse[static_cast<size_t>(bh) * p.N + q_idx] = (m_ref + __log2f(l_run)) * 0.6931471805599453f;
+  return true;
 }
 
 template <int D, bool kNegScale>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = Cfg<D>;
   constexpr int SK = C::kStagesK;
   constexpr int SV = C::kStagesV;
@@ -402,17 +418,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int unit = p.num_units - 1 - static_cast<int>(blockIdx.y);  // heaviest first
-  const int q0 = unit * kUnitM;
-  int n_t[kTilesPerCta];
-#pragma unroll
-  for (int t = 0; t < kTilesPerCta; ++t) n_t[t] = key_tiles_for(q0 + kTileM * t, p.N, p.causal);
-  const int n_max = max(n_t[0], n_t[1]);  // n_t[0] >= 1 always
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < kTilesPerCta; ++t) {
       mbar_init(bars.q_full(t), 1);
+      mbar_init(bars.q_empty(t), 1);
       mbar_init(bars.s_full(t), 1);
       mbar_init(bars.p_full(t), kRowThreadsPerTile / 32);  // one arrival per warp
       mbar_init(bars.o_done(t), 1);
@@ -437,7 +447,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -455,166 +464,231 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp < kLoadWarp) {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
-    softmax_tile<D, kNegScale>(t, n_t[t], q0 + kTileM * t, tmem, sQ + t * C::kQBytes, bars, wctx,
-                               &tm_o, p, bh);
+    uint32_t s_uses = 0, o_uses = 0;  // phases of s_full(t) / o_done(t) consumed so far
+    for (int r = 0;; ++r) {
+      const int idx = unit_index(r);
+      if (idx >= p.total_units) break;
+      const Unit u = unit_at(idx, p);
+      const int n = t == 0 ? u.n[0] : u.n[1];
+      if (n == 0) continue;
+      if (!softmax_tile<D, kNegScale>(t, n, u.q0 + kTileM * t, u.bh, tmem, bars, wctx, p, s_uses,
+                                      o_uses))
+        break;
+    }
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------------------ Q, K producer
     if (lane == 0) {
-      int issued = 0;  // K_j copies issued for j < issued
-      bool q_issued[kTilesPerCta] = {false, false};
-      for (int j = 0; j < n_max; ++j) {
-        const int s = j % SK;
-        if (j >= SK && !wait_bar(bars.k_empty(s), (static_cast<uint32_t>(j / SK) & 1u) ^ 1u, wctx))
-          break;
-        if (j == 0) {  // Q_A first: S_A(0) needs only Q_A and K_0
-          mbar_arrive_expect_tx(bars.q_full(0), C::kQBytes);
+      uint32_t kc = 0;                     // K tiles issued so far (ring position)
+      uint32_t qc[kTilesPerCta] = {0, 0};  // Q tiles issued so far, per tile slot
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int idx = unit_index(r);
+        if (idx >= p.total_units) break;
+        const Unit u = unit_at(idx, p);
+        const int n_max = max(u.n[0], u.n[1]);
+        for (int j = 0; j < n_max; ++j) {
+          const int s = static_cast<int>(kc % SK);
+          if (kc >= static_cast<uint32_t>(SK) &&
+              !wait_bar(bars.k_empty(s), parity_of(kc / SK - 1), wctx)) {
+            ok = false;
+            break;
+          }
+          if (j == 0) {
+            // Q_t of this unit replaces the previous unit's once every S_t
+            // MMA that read it has completed (q_empty).
+#pragma unroll
+            for (int t = 0; t < kTilesPerCta; ++t) {
+              if (!ok || u.n[t] == 0) continue;
+              if (qc[t] > 0 && !wait_bar(bars.q_empty(t), parity_of(qc[t] - 1), wctx)) {
+                ok = false;
+                continue;
+              }
+              mbar_arrive_expect_tx(bars.q_full(t), C::kQBytes);
+#pragma unroll
+              for (int b = 0; b < D / 64; ++b)
+                tma_load_3d(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t), 64 * b,
+                            u.q0 + kTileM * t, u.bh);
+              ++qc[t];
+            }
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(sQ + b * kSwBlockBytes, &tm_q, bars.q_full(0), 64 * b, q0, bh);
-          q_issued[0] = true;
-        }
-        mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b)
-          tma_load_3d(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s), 64 * b,
-                      j * kBlockN, bh);
-        issued = j + 1;
-        if (j == 0 && n_t[1] > 0) {
-          mbar_arrive_expect_tx(bars.q_full(1), C::kQBytes);
-#pragma unroll
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(sQ + C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(1), 64 * b,
-                        q0 + kTileM, bh);
-          q_issued[1] = true;
+            tma_load_3d(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s), 64 * b,
+                        j * kBlockN, u.bh);
+          ++kc;
         }
       }
       // Drain: every copy issued must land before the CTA may exit.  The last
-      // copy into stage s is the largest j < issued with j % SK == s.
+      // copy into stage s is the largest count < kc congruent to s mod SK.
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t)
-        if (q_issued[t]) wait_bar_drain(bars.q_full(t), 0, wctx);
+        if (qc[t] > 0) wait_bar_drain(bars.q_full(t), parity_of(qc[t] - 1), wctx);
 #pragma unroll
       for (int s = 0; s < SK; ++s) {
-        if (issued > s) {
-          const int jl = issued - 1 - ((issued - 1 - s) % SK);
-          wait_bar_drain(bars.k_full(s), static_cast<uint32_t>(jl / SK) & 1u, wctx);
+        if (kc > static_cast<uint32_t>(s)) {
+          const uint32_t last = kc - 1 - ((kc - 1 - s) % SK);
+          wait_bar_drain(bars.k_full(s), parity_of(last / SK), wctx);
         }
       }
     }
   } else if (warp == kLoadVWarp) {
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
-      int issued = 0;  // V_j copies issued (or deliberately skipped) for j < issued
+      uint32_t vc = 0;  // V tiles issued (or deliberately skipped) so far
       bool v0_skipped = false;
-      for (int j = 0; j < n_max; ++j) {
-        const int s = j % SV;
-        if (j >= SV && !wait_bar(bars.v_empty(s), (static_cast<uint32_t>(j / SV) & 1u) ^ 1u, wctx))
-          break;
-        issued = j + 1;
-        if (j == 0 && (p.inject & kInjectSkipFirstV)) {
-          v0_skipped = true;
-          continue;
-        }
-        mbar_arrive_expect_tx(bars.v_full(s), C::kKVBytes);
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int idx = unit_index(r);
+        if (idx >= p.total_units) break;
+        const Unit u = unit_at(idx, p);
+        const int n_max = max(u.n[0], u.n[1]);
+        for (int j = 0; j < n_max; ++j) {
+          const int s = static_cast<int>(vc % SV);
+          if (vc >= static_cast<uint32_t>(SV) &&
+              !wait_bar(bars.v_empty(s), parity_of(vc / SV - 1), wctx)) {
+            ok = false;
+            break;
+          }
+          ++vc;
+          if (vc == 1 && (p.inject & kInjectSkipFirstV)) {
+            v0_skipped = true;
+            continue;
+          }
+          mbar_arrive_expect_tx(bars.v_full(s), C::kKVBytes);
 #pragma unroll
-        for (int b = 0; b < D / 64; ++b)
-          tma_load_3d(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s), 64 * b,
-                      j * kBlockN, bh);
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s), 64 * b,
+                        j * kBlockN, u.bh);
+        }
       }
 #pragma unroll
       for (int s = 0; s < SV; ++s) {
-        if (issued > s) {
-          const int jl = issued - 1 - ((issued - 1 - s) % SV);
-          if (!(jl == 0 && v0_skipped))
-            wait_bar_drain(bars.v_full(s), static_cast<uint32_t>(jl / SV) & 1u, wctx);
+        if (vc > static_cast<uint32_t>(s)) {
+          const uint32_t last = vc - 1 - ((vc - 1 - s) % SV);
+          if (!(last == 0 && v0_skipped))
+            wait_bar_drain(bars.v_full(s), parity_of(last / SV), wctx);
         }
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      // Descriptor halves.  Every operand sits at a fixed SMEM address, so
-      // the low halves of all descriptors are a base plus compile-time
-      // offsets (>> 4) and each MMA issue costs a couple of integer adds.
-      constexpr uint32_t kHi = desc_hi_sw128(1024);
-      const uint32_t q_lo = desc_lo(sQ, 16);
-      const uint32_t k_lo = desc_lo(sK, 16);
-      const uint32_t v_lo = desc_lo(sV, kSwBlockBytes);
-      // K-major slice kk of a [128 x D] tile: block kk/4, 32 bytes per slice.
-      auto kmaj_off = [](int kk) -> uint32_t {
-        return ((kk >> 2) * kSwBlockBytes + (kk & 3) * 32) >> 4;
-      };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t a_lo = q_lo + ((t * C::kQBytes) >> 4);
-        const uint32_t b_lo = k_lo + (((j % SK) * C::kKVBytes) >> 4);
-        const uint32_t d_tmem = tmem + C::kColS + 128u * t;
+    // The whole warp runs this loop on warp-uniform values and one lane,
+    // elected once, issues every tcgen05 operation: uniform operands stay in
+    // uniform registers and an MMA issues in ~40 cycles, faster than the
+    // tensor core retires one (64 cycles for 128x128x16), so the issuer can
+    // run ahead.  The same lane must issue the MMAs and the commits: a
+    // commit tracks only the MMAs of its own thread.
+    const bool leader = elect_one_sync();
+    // Descriptor halves: every operand sits at a fixed SMEM address, so the
+    // low halves of all descriptors are a base plus compile-time offsets.
+    constexpr uint32_t kHi = desc_hi_sw128(1024);
+    const uint32_t q_lo = desc_lo(sQ, 16);
+    const uint32_t k_lo = desc_lo(sK, 16);
+    const uint32_t v_lo = desc_lo(sV, kSwBlockBytes);
+    // K-major slice kk of a [128 x D] tile: block kk/4, 32 bytes per slice.
+    auto kmaj_off = [](int kk) -> uint32_t {
+      return ((kk >> 2) * kSwBlockBytes + (kk & 3) * 32) >> 4;
+    };
+    auto commit = [&](uint32_t bar) {
+      if (leader) umma_commit(bar);
+      __syncwarp();
+    };
+    auto issue_s = [&](int t, uint32_t k_stage) {  // S_t = Q_t K^T
+      const uint32_t a_lo = q_lo + ((t * C::kQBytes) >> 4);
+      const uint32_t b_lo = k_lo + ((k_stage * C::kKVBytes) >> 4);
+      const uint32_t d_tmem = tmem + C::kColS + 128u * t;
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss_lohi(d_tmem, a_lo + kmaj_off(kk), kHi, b_lo + kmaj_off(kk), kHi, C::kIdescQK,
                        kk > 0 ? 1u : 0u);
-        umma_commit(bars.s_full(t));
-      };
-      auto issue_pv = [&](int t, int j) {
-        // V slice kk: 16 key rows of 128 bytes.
-        const uint32_t b_lo = v_lo + (((j % SV) * C::kKVBytes) >> 4);
-        const uint32_t p_tmem = tmem + C::kColS + 128u * t;
-        const uint32_t d_tmem = tmem + C::kColO + static_cast<uint32_t>(D) * t;
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, uint32_t v_stage, bool first) {  // O_t (+)= P_t V
+      const uint32_t b_lo = v_lo + ((v_stage * C::kKVBytes) >> 4);
+      const uint32_t p_tmem = tmem + C::kColS + 128u * t;
+      const uint32_t d_tmem = tmem + C::kColO + static_cast<uint32_t>(D) * t;
+      const uint32_t acc0 = first ? 0u : 1u;
+      if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
+        for (int kk = 0; kk < kBlockN / 16; ++kk)  // V slice kk: 16 key rows of 128 bytes
           umma_ts_lohi(d_tmem, p_tmem + 8u * kk, b_lo + ((kk * 16 * 128) >> 4), kHi, C::kIdescPV,
                        kk > 0 ? 1u : acc0);
-      };
-      auto wait_k = [&](int j) {
-        return wait_bar(bars.k_full(j % SK), static_cast<uint32_t>(j / SK) & 1u, wctx);
-      };
-
-      bool ok = wait_k(0) && wait_bar(bars.q_full(0), 0, wctx);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0, 0);
-        if (n_t[1] > 0) {
-          ok = wait_bar(bars.q_full(1), 0, wctx);
-          if (ok) {
-            tc_fence_after_sync();
-            issue_s(1, 0);
-          }
-        }
-        if (ok) umma_commit(bars.k_empty(0));
       }
-      // Issuing a tcgen05.mma waits for room in the tensor core's queue, so
-      // this thread runs only a little ahead of the MMAs: every wait, fence
-      // or commit between two MMA groups is tensor-core idle time.  All
-      // waits of an iteration therefore come first (the TMA waits are
-      // normally already satisfied), and commits are batched after groups.
+      __syncwarp();
+    };
+
+    uint32_t kc = 0, vc = 0;             // ring positions consumed
+    uint32_t qc[kTilesPerCta] = {0, 0};  // Q loads consumed per tile slot
+    uint32_t pc[kTilesPerCta] = {0, 0};  // p_full phases consumed per tile
+    bool ok = true;
+    // All waits of an iteration come first (the TMA waits are normally
+    // already satisfied) and commits follow the group they cover, so the
+    // issuer stays ahead of the tensor core across group boundaries.
+    for (int r = 0; ok; ++r) {
+      const int idx = unit_index(r);
+      if (idx >= p.total_units) break;
+      const Unit u = unit_at(idx, p);
+      const int n_max = max(u.n[0], u.n[1]);
+      // j = 0: S_t(0) for every active tile.
+      if (!warp_wait_bar(bars.k_full(kc % SK), parity_of(kc / SK), wctx)) break;
+#pragma unroll
+      for (int t = 0; t < kTilesPerCta; ++t) {
+        if (!ok || u.n[t] == 0) continue;
+        if (!warp_wait_bar(bars.q_full(t), parity_of(qc[t]), wctx)) {
+          ok = false;
+          continue;
+        }
+        ++qc[t];
+        issue_s(t, kc % SK);
+        commit(bars.s_full(t));
+        if (u.n[t] == 1) commit(bars.q_empty(t));  // last S_t of the unit
+      }
+      if (!ok) break;
+      commit(bars.k_empty(kc % SK));
+      ++kc;
       for (int j = 0; ok && j < n_max; ++j) {
-        const int s = j % SV;
         const bool more = j + 1 < n_max;
-        if (!wait_bar(bars.v_full(s), static_cast<uint32_t>(j / SV) & 1u, wctx)) break;
-        if (more && !wait_k(j + 1)) break;
+        if (!warp_wait_bar(bars.v_full(vc % SV), parity_of(vc / SV), wctx) ||
+            (more && !warp_wait_bar(bars.k_full(kc % SK), parity_of(kc / SK), wctx))) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int t = 0; t < kTilesPerCta; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!wait_bar(bars.p_full(t), static_cast<uint32_t>(j) & 1u, wctx)) {
+          const int n = t == 0 ? u.n[0] : u.n[1];
+          if (!ok || j >= n) continue;
+          if (!warp_wait_bar(bars.p_full(t), parity_of(pc[t]), wctx)) {
             ok = false;
-            break;
+            continue;
           }
+          ++pc[t];
           tc_fence_after_sync();
-          issue_pv(t, j);
-          if (j + 1 < n_t[t]) {
-            issue_s(t, j + 1);  // commits s_full(t), which also covers P_t(j) V_j
+          issue_pv(t, vc % SV, j == 0);
+          if (j + 1 < n) {
+            // S_t(j+1) overwrites P_t(j); MMAs of one thread run in issue order.
+            issue_s(t, kc % SK);
+            commit(bars.s_full(t));  // also covers P_t(j) V_j: O_t is current
+            if (j + 2 == n) commit(bars.q_empty(t));  // last S_t of the unit
           } else {
-            umma_commit(bars.o_done(t));
+            commit(bars.o_done(t));
           }
         }
         if (!ok) break;
-        umma_commit(bars.v_empty(s));                 // V_j: both P.V products issued
-        if (more) umma_commit(bars.k_empty((j + 1) % SK));  // K_j+1: both S MMAs issued
+        commit(bars.v_empty(vc % SV));  // V_j: every P.V product issued
+        ++vc;
+        if (more) {
+          commit(bars.k_empty(kc % SK));  // K_j+1: every S MMA issued
+          ++kc;
+        }
       }
-      // Drain: wait for every MMA issued by this thread.
-      umma_commit(bars.mma_done());
-      wait_bar_drain(bars.mma_done(), 0, wctx);
     }
+    // Drain: wait for every MMA issued by this warp.
+    commit(bars.mma_done());
+    wait_bar_drain(bars.mma_done(), 0, wctx);
   }
 
   // ------------------------------------------------------------ teardown
