@@ -24,7 +24,7 @@
 //   warp 11     idle (it completes the third warpgroup)
 // The third warpgroup hands most of its registers to the two softmax
 // warpgroups (setmaxnreg): 384 threads launch with 168 registers each
-// (64512 in all); afterwards 256 x 216 + 128 x 72 = 64512 are in use.
+// (64512 in all); afterwards 256 x 200 + 128 x 104 = 64512 are in use.
 //
 // The tensor core alternates between the tiles: while the softmax warps of A
 // turn S_A(j) into P_A(j), it computes P_B(j-1) V_(j-1) and S_B(j), and vice
@@ -65,8 +65,8 @@ constexpr int kUnitM = kTileM * kTilesPerCta;  // query rows per work unit
 constexpr int kBlockN = 128;                   // keys per K/V tile
 constexpr int kNumThreads = 384;
 constexpr uint32_t kLaunchRegs = 168;   // 65536 / (3 warps per sub-partition x 32 x 4)
-constexpr uint32_t kSoftmaxRegs = 216;  // after setmaxnreg.inc
-constexpr uint32_t kControlRegs = 72;   // after setmaxnreg.dec
+constexpr uint32_t kSoftmaxRegs = 200;  // after setmaxnreg.inc
+constexpr uint32_t kControlRegs = 104;  // after setmaxnreg.dec
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kNumThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 static_assert(2 * kSoftmaxRegs + kControlRegs <= 512, "per-sub-partition register file");
@@ -282,24 +282,21 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
     }
 
     // Row extreme of the raw scores (max for a positive scale, min for a
-    // negative one), four independent 3-input chains.
-    float e0 = s[0], e1 = s[1], e2 = s[2], e3 = s[3];
+    // negative one), eight independent chains.  (The three-input min/max
+    // forms of sm_100+ were dropped: inside this kernel they produced NaN for
+    // some register allocations, while two-input chains are exact.)
+    float ev[8];
 #pragma unroll
-    for (int i = 4; i < kBlockN; i += 8) {
-      if (kNegScale) {
-        e0 = fmin3(e0, s[i], s[i + 1]);
-        e1 = fmin3(e1, s[i + 2], s[i + 3]);
-        e2 = fmin3(e2, s[i + 4], s[i + 5]);
-        e3 = fmin3(e3, s[i + 6], s[i + 7]);
-      } else {
-        e0 = fmax3(e0, s[i], s[i + 1]);
-        e1 = fmax3(e1, s[i + 2], s[i + 3]);
-        e2 = fmax3(e2, s[i + 4], s[i + 5]);
-        e3 = fmax3(e3, s[i + 6], s[i + 7]);
-      }
-    }
-    const float ext =
-        kNegScale ? fminf(fminf(e0, e1), fminf(e2, e3)) : fmaxf(fmaxf(e0, e1), fmaxf(e2, e3));
+    for (int k = 0; k < 8; ++k) ev[k] = s[k];
+#pragma unroll
+    for (int i = 8; i < kBlockN; i += 8)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ev[k] = kNegScale ? fminf(ev[k], s[i + k]) : fmaxf(ev[k], s[i + k]);
+#pragma unroll
+    for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) ev[k] = kNegScale ? fminf(ev[k], ev[k + w]) : fmaxf(ev[k], ev[k + w]);
+    const float ext = ev[0];
     const float m_tile = ext * c;  // max of the scaled scores of this tile
 
     // Lazy rescale: move the reference only when the tile max exceeds it by
@@ -668,6 +665,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           ++pc[t];
           tc_fence_after_sync();
           issue_pv(t, vc % SV, j == 0);
+          // V_j is free once the last tile that reads it has its P.V issued
+          // (released before the S MMA that follows, to refill the ring early).
+          if (t == kTilesPerCta - 1 || j >= u.n[kTilesPerCta - 1]) commit(bars.v_empty(vc % SV));
           if (j + 1 < n) {
             // S_t(j+1) overwrites P_t(j); MMAs of one thread run in issue order.
             issue_s(t, kc % SK);
@@ -678,7 +678,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
         }
         if (!ok) break;
-        commit(bars.v_empty(vc % SV));  // V_j: every P.V product issued
         ++vc;
         if (more) {
           commit(bars.k_empty(kc % SK));  // K_j+1: every S MMA issued
