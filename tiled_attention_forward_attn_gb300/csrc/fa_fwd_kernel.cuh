@@ -475,6 +475,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == kLoadWarp) {
     // ------------------------------------------------------------ Q, K producer
     if (lane == 0) {
+      // K/V tiles are read again by every query unit of the same head: keep
+      // them in L2.  Q is read once.
+      const uint64_t keep = make_l2_policy_evict_last();
+      const uint64_t once = make_l2_policy_evict_first();
       uint32_t kc = 0;                     // K tiles issued so far (ring position)
       uint32_t qc[kTilesPerCta] = {0, 0};  // Q tiles issued so far, per tile slot
       bool ok = true;
@@ -503,8 +507,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               mbar_arrive_expect_tx(bars.q_full(t), C::kQBytes);
 #pragma unroll
               for (int b = 0; b < D / 64; ++b)
-                tma_load_3d(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t), 64 * b,
-                            u.q0 + kTileM * t, u.bh);
+                tma_load_3d_hint(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t),
+                                 64 * b, u.q0 + kTileM * t, u.bh, once);
               ++qc[t];
             }
             if (!ok) break;
@@ -512,8 +516,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s), 64 * b,
-                        j * kBlockN, u.bh);
+            tma_load_3d_hint(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s),
+                             64 * b, j * kBlockN, u.bh, keep);
           ++kc;
         }
       }
@@ -533,6 +537,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == kLoadVWarp) {
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
+      const uint64_t keep = make_l2_policy_evict_last();
       uint32_t vc = 0;  // V tiles issued (or deliberately skipped) so far
       bool v0_skipped = false;
       bool ok = true;
@@ -556,8 +561,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           mbar_arrive_expect_tx(bars.v_full(s), C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s), 64 * b,
-                        j * kBlockN, u.bh);
+            tma_load_3d_hint(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s),
+                             64 * b, j * kBlockN, u.bh, keep);
         }
       }
 #pragma unroll
