@@ -126,6 +126,25 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+def reduce_max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over all ranks (identity when the
+    process group is not initialised).  Used for the per-rank timings."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `flops_per_step`;
+    the job takes the slowest rank's `ms`."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -267,21 +286,16 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
 
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([kernel_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        kernel_ms, e2e_ms = float(t[0]), float(t[1])
+    kernel_ms, e2e_ms = reduce_max_over_ranks([kernel_ms, e2e_ms], device=dev)
 
     if rank == 0:
         peaks, peaks_src = load_peaks()
         flops_step = w.flops
-        value = world * flops_step * args.steps / (kernel_ms * 1e-3) / 1e12
+        value = job_tflops(world, flops_step, args.steps, kernel_ms)
         avg_launch_s = kernel_ms * 1e-3 / args.steps
         achieved = flops_step / avg_launch_s / 1e12
         peak = float(peaks["bf16_tflops"])
-        e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+        e2e_value = job_tflops(world, flops_step, e2e_steps, e2e_ms)
 
         cpu = None
         if world == 1 and not args.skip_cpu_baseline:
