@@ -62,6 +62,12 @@ def _load():
             lib.oracle_scores.argtypes = [_u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                           ctypes.c_int64, _f64p]
+            lib.oracle_attention_rect.restype = ctypes.c_int
+            lib.oracle_attention_rect.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_int, ctypes.c_double, _i64p,
+                                                  ctypes.c_int64, _f64p, _f64p, _f64p,
+                                                  ctypes.c_int]
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_attention.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_double,
@@ -134,36 +140,39 @@ def attention(q, k, v, causal: bool, scale: float, rows=None,
               return_probs: bool = False, threads: int = 0):
     """Exact attention forward on bf16 inputs, in fp64.
 
-    q, k, v: uint16 bf16 bit patterns shaped ``[..., N, d]`` (leading dims
-    are flattened into independent slices).  ``rows``: optional 1-D array of
-    query indices evaluated in every slice (default: all).  Returns
+    q: uint16 bf16 bit patterns shaped ``[..., Nq, d]``; k, v: ``[..., Nk, d]``
+    (leading dims equal and flattened into independent slices).  Causal
+    masking is aligned to the end of the keys: query i sees keys
+    ``0 .. Nk - Nq + i`` (``0 .. i`` when Nq == Nk).  ``rows``: optional 1-D
+    array of query indices evaluated in every slice (default: all).  Returns
     ``(O, LSE)`` (and ``P`` if ``return_probs``) as fp64 arrays shaped
-    ``[..., n_rows, d]`` / ``[..., n_rows]`` / ``[..., n_rows, N]``.
+    ``[..., n_rows, d]`` / ``[..., n_rows]`` / ``[..., n_rows, Nk]``.
     """
     lib = _load()
     q, k, v = _u16(q), _u16(k), _u16(v)
-    if q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must share one shape [..., N, d]")
+    if k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+        raise ValueError("q [..., Nq, d] and k, v [..., Nk, d] disagree")
     lead = q.shape[:-2]
-    N, d = q.shape[-2:]
+    Nq, d = q.shape[-2:]
+    Nk = k.shape[-2]
     BH = int(np.prod(lead)) if lead else 1
     if rows is None:
         rows_arr = None
-        n_rows = N
+        n_rows = Nq
     else:
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         n_rows = rows_arr.size
     o = np.empty((BH, n_rows, d))
     lse = np.empty((BH, n_rows))
-    p = np.empty((BH, n_rows, N)) if return_probs else None
-    rc = lib.oracle_attention(
-        _ptr(q, _u16p), _ptr(k, _u16p), _ptr(v, _u16p), BH, N, d, int(bool(causal)),
+    p = np.empty((BH, n_rows, Nk)) if return_probs else None
+    rc = lib.oracle_attention_rect(
+        _ptr(q, _u16p), _ptr(k, _u16p), _ptr(v, _u16p), BH, Nq, Nk, d, int(bool(causal)),
         float(scale), None if rows_arr is None else _ptr(rows_arr, _i64p), n_rows,
         _ptr(o, _f64p), _ptr(lse, _f64p), None if p is None else _ptr(p, _f64p), int(threads))
     if rc != 0:
-        raise ValueError(f"oracle_attention failed with code {rc}")
+        raise ValueError(f"oracle_attention_rect failed with code {rc}")
     o = o.reshape(lead + (n_rows, d))
     lse = lse.reshape(lead + (n_rows,))
     if return_probs:
-        return o, lse, p.reshape(lead + (n_rows, N))
+        return o, lse, p.reshape(lead + (n_rows, Nk))
     return o, lse

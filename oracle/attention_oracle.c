@@ -14,7 +14,8 @@
  * Readings of points the pages leave open:
  *   - the scale multiplies the fp64 dot product (it is not folded into Q);
  *   - LSE_i = m_i + ln(l_i) of the scaled, masked scores (natural log);
- *   - causal masking is square and top-left aligned (query i sees keys 0..i).
+ *   - causal masking: query i of Nq sits at position Nk - Nq + i of the Nk
+ *     keys and sees keys 0..Nk-Nq+i (square attention: keys 0..i).
  *
  * Inputs are bf16 bit patterns (uint16); each is widened to fp64 exactly.
  * Every floating-point step below runs in fp64.
@@ -99,26 +100,30 @@ void oracle_scores(const uint16_t *q, const uint16_t *k, int64_t nq,
 }
 
 /*
- * Attention forward for selected rows of every (batch, head) slice.
- *   q, k, v : [BH][N][d] bf16 bit patterns
- *   rows    : n_rows query indices (each in [0, N)), applied to every slice;
- *             NULL means all rows (n_rows must then equal N)
+ * Attention forward for selected query rows of every (batch, head) slice,
+ * with Nq queries against Nk keys.  Causal masking is aligned to the end of
+ * the key sequence: query i sits at position Nk - Nq + i and sees keys
+ * j <= Nk - Nq + i (for Nq == Nk this is the square rule j <= i).
+ *   q       : [BH][Nq][d] bf16 bit patterns
+ *   k, v    : [BH][Nk][d] bf16 bit patterns
+ *   rows    : n_rows query indices (each in [0, Nq)), applied to every slice;
+ *             NULL means all rows (n_rows must then equal Nq)
  *   o_out   : [BH][n_rows][d] fp64,   O_i = sum_j P_ij v_j
  *   lse_out : [BH][n_rows]   fp64,   LSE_i = m_i + ln(l_i)
- *   p_out   : optional [BH][n_rows][N] fp64 probabilities (may be NULL)
+ *   p_out   : optional [BH][n_rows][Nk] fp64 probabilities (may be NULL)
  * Returns 0, or -1 on bad arguments / -2 on allocation failure.
  */
-int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     int64_t BH, int64_t N, int64_t d, int causal,
-                     double scale, const int64_t *rows, int64_t n_rows,
-                     double *o_out, double *lse_out, double *p_out,
-                     int n_threads)
+int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                          double scale, const int64_t *rows, int64_t n_rows,
+                          double *o_out, double *lse_out, double *p_out, int n_threads)
 {
     if (!q || !k || !v || !o_out || !lse_out) return -1;
-    if (BH <= 0 || N <= 0 || d <= 0 || n_rows <= 0) return -1;
-    if (!rows && n_rows != N) return -1;
+    if (BH <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || n_rows <= 0) return -1;
+    if (causal && Nq > Nk) return -1; /* some query would see no key */
+    if (!rows && n_rows != Nq) return -1;
     for (int64_t r = 0; rows && r < n_rows; ++r)
-        if (rows[r] < 0 || rows[r] >= N) return -1;
+        if (rows[r] < 0 || rows[r] >= Nq) return -1;
 
     int failed = 0;
     int64_t tasks = BH * n_rows;
@@ -127,8 +132,8 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 #pragma omp parallel
 #endif
     {
-        double *s = (double *)malloc((size_t)N * sizeof(double));
-        double *p = (double *)malloc((size_t)N * sizeof(double));
+        double *s = (double *)malloc((size_t)Nk * sizeof(double));
+        double *p = (double *)malloc((size_t)Nk * sizeof(double));
         if (!s || !p) {
 #ifdef _OPENMP
 #pragma omp atomic write
@@ -143,30 +148,51 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             int64_t bh = task / n_rows;
             int64_t r = task % n_rows;
             int64_t i = rows ? rows[r] : r;
-            const uint16_t *qh = q + (bh * N + i) * d;
-            const uint16_t *kh = k + bh * N * d;
-            const uint16_t *vh = v + bh * N * d;
+            const uint16_t *qh = q + (bh * Nq + i) * d;
+            const uint16_t *kh = k + bh * Nk * d;
+            const uint16_t *vh = v + bh * Nk * d;
 
-            oracle_score_row(qh, kh, i, N, d, scale, causal, s);
+            /* position of query i among the keys (end-aligned) */
+            oracle_score_row(qh, kh, Nk - Nq + i, Nk, d, scale, causal, s);
             double m, l;
-            oracle_safe_softmax(s, N, NULL, p, &m, &l);
+            oracle_safe_softmax(s, Nk, NULL, p, &m, &l);
 
             double *o = o_out + (bh * n_rows + r) * d;
             for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
-            for (int64_t j = 0; j < N; ++j) {
+            for (int64_t j = 0; j < Nk; ++j) {
                 if (p[j] == 0.0) continue; /* masked keys add 0 * v_j */
                 for (int64_t t = 0; t < d; ++t)
                     o[t] += p[j] * oracle_bf16_to_double(vh[j * d + t]);
             }
             lse_out[bh * n_rows + r] = m + log(l);
             if (p_out)
-                memcpy(p_out + (bh * n_rows + r) * N, p,
-                       (size_t)N * sizeof(double));
+                memcpy(p_out + (bh * n_rows + r) * Nk, p,
+                       (size_t)Nk * sizeof(double));
         }
         free(s);
         free(p);
     }
     return failed ? -2 : 0;
+}
+
+/*
+ * Square self-attention (Nq == Nk == N): the same computation.
+ *   q, k, v : [BH][N][d] bf16 bit patterns
+ *   rows    : n_rows query indices (each in [0, N)), applied to every slice;
+ *             NULL means all rows (n_rows must then equal N)
+ *   o_out   : [BH][n_rows][d] fp64,   O_i = sum_j P_ij v_j
+ *   lse_out : [BH][n_rows]   fp64,   LSE_i = m_i + ln(l_i)
+ *   p_out   : optional [BH][n_rows][N] fp64 probabilities (may be NULL)
+ * Returns 0, or -1 on bad arguments / -2 on allocation failure.
+ */
+int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t BH, int64_t N, int64_t d, int causal,
+                     double scale, const int64_t *rows, int64_t n_rows,
+                     double *o_out, double *lse_out, double *p_out,
+                     int n_threads)
+{
+    return oracle_attention_rect(q, k, v, BH, N, N, d, causal, scale, rows, n_rows,
+                                 o_out, lse_out, p_out, n_threads);
 }
 
 /* Threads OpenMP would use by default (1 without OpenMP). */

@@ -52,6 +52,26 @@ def merge_stats(m_a, l_a, m_b, l_b):
     return m, l_a * np.exp(m_a - m) + l_b * np.exp(m_b - m)
 
 
+def combine_partials(o_parts, lse_parts):
+    """Merge attention results computed over disjoint key subsets.
+
+    o_parts[s] is the normalised output of subset s and lse_parts[s] its
+    log-sum-exp (-inf for a subset with no visible key).  The block-merge
+    identity (page 1 eq. (20); "Online Softmax and FlashAttention") with
+    l_s = e^(LSE_s - m_s) gives LSE = ln sum_s e^(LSE_s) and
+    O = sum_s e^(LSE_s - LSE) O_s.  Shapes: o_parts [S, ..., d],
+    lse_parts [S, ...]; returns (O [..., d], LSE [...]).
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = lse_parts.max(axis=0)
+    w = np.exp(lse_parts - m)  # 0 for empty subsets
+    total = w.sum(axis=0)
+    lse = m + np.log(total)
+    o = (np.where(w[..., None] > 0, o_parts, 0.0) * (w / total)[..., None]).sum(axis=0)
+    return o, lse
+
+
 def stream_stats(x):
     """Online max/sum over a vector one element at a time (the prefix
     recurrence of "Online Softmax and FlashAttention"): m_t = max(m_{t-1},
