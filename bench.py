@@ -38,11 +38,15 @@ import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOPS & % of GB300 BF16 tensor peak (N=4096,d=128,causal)"
 UNIT = "TFLOPS"
+# The split-KV decode workloads are bound by HBM: GB/s of algorithmic bytes.
+DECODE_METRIC = "split-KV decode attention GB/s of algorithmic HBM bytes & % of measured HBM bandwidth"
+DECODE_UNIT = "GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 # Per-launch DRAM traffic of the attention kernel on this workload, from an
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum); None until the
 # kernel it was taken on is the one benchmarked.
+NCU_TRAFFIC_BYTES_DECODE = {}  # workload name -> bytes per launch pair, from ncu
 NCU_TRAFFIC_BYTES = 131_094_272  # 122.52 MB read + 8.57 MB written (profiles/fa_fwd_kernel_b2h16n4096d128_causal.md)
 
 
@@ -152,6 +156,20 @@ def dist_setup():
     return world, rank, local
 
 
+def cpu_oracle_sample_decode(w, qkv, heads: int, threads: int = 0):
+    """Time the fp64 oracle on the first `heads` (batch, head) slices of a
+    decode workload; returns (seconds, algorithmic bytes of those slices,
+    slices, cores)."""
+    import oracle
+
+    q, k, v = (np.ascontiguousarray(a.reshape(w.B * w.H, *a.shape[2:])[:heads]) for a in qkv)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.causal, w.scale, threads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = w.io_bytes * heads / (w.B * w.H)
+    return dt, nbytes, heads, oracle.max_threads() if threads <= 0 else threads
+
+
 def cpu_oracle_sample(w, qkv, rows_per_head: int, seed: int, threads: int = 0):
     """Time the fp64 oracle on a fixed seeded sample of query rows.
 
@@ -175,6 +193,8 @@ def run_reference(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
+    if isinstance(w, workloads.DecodeWorkload):
+        return run_reference_decode(args, w)
     rows_per_head = args.ref_rows
     qkv = workloads.generate(w)
     times = []
@@ -205,6 +225,35 @@ def run_reference(args, w):
     return 0
 
 
+def run_reference_decode(args, w):
+    world, _, _ = dist_setup()
+    qkv = workloads.generate_decode(w)
+    times, nbytes, heads, cores = [], 0.0, 1, 0
+    for i in range(args.warmup + args.steps):
+        dt, nbytes, heads, cores = cpu_oracle_sample_decode(w, qkv, heads=2)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    sample = (f"{heads} of {w.B * w.H} (batch, head) slices per step, all {w.Nq} queries "
+              f"against {w.Nk} keys, fp64 oracle, {cores} threads")
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": DECODE_UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": DECODE_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args, w):
     import torch
 
@@ -219,15 +268,23 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     fa.load_library()
 
-    q, k, v = workloads.generate(w)
+    decode = isinstance(w, workloads.DecodeWorkload)
+    q, k, v = workloads.generate_decode(w) if decode else workloads.generate(w)
     qd, kd, vd = (workloads.as_torch_bf16(a).to(dev) for a in (q, k, v))
     o = torch.empty_like(qd)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    lse = torch.empty(tuple(qd.shape[:3]), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if decode:
+        ws_bytes = fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, 0)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        n_splits = fa.fa_fwd_splitkv_num_splits(w.B, w.H, w.Nq, w.Nk, w.d, 0)
 
-    def step():
-        fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+        def step():
+            fa.fa_fwd_splitkv(qd, kd, vd, o, lse, w.causal, w.scale, 0, workspace, stream)
+    else:
+        def step():
+            fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
 
     for _ in range(args.warmup):
         step()
@@ -263,7 +320,7 @@ def run_ours(args, w):
     hq, hk, hv = (workloads.as_torch_bf16(a).pin_memory() for a in (q, k, v))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = 3 * hq.numel() * hq.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
     def e2e_step():
@@ -288,7 +345,45 @@ def run_ours(args, w):
 
     kernel_ms, e2e_ms = reduce_max_over_ranks([kernel_ms, e2e_ms], device=dev)
 
-    if rank == 0:
+    if rank == 0 and decode:
+        peaks, peaks_src = load_peaks()
+        per_step = float(w.io_bytes)
+        value = world * per_step * args.steps / (kernel_ms * 1e-3) / 1e9
+        achieved = per_step / (kernel_ms * 1e-3 / args.steps) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        e2e_value = world * per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9
+        cpu = None
+        if world == 1 and not args.skip_cpu_baseline:
+            dt, nbytes, heads, cores = cpu_oracle_sample_decode(w, (q, k, v), heads=2)
+            cpu = {"value": nbytes / dt / 1e9, "unit": DECODE_UNIT, "cores": cores,
+                   "kind": "oracle",
+                   "sample": (f"{heads} of {w.B * w.H} (batch, head) slices, all {w.Nq} "
+                              f"queries against {w.Nk} keys, fp64 oracle, {dt:.1f} s")}
+        line = {
+            "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": kernel_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": w.causal, "splits": n_splits,
+                       "l2": "flushed between launches (256 MiB write, untimed); K+V exceed L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peaks_src} hbm_gbs",
+                         "timed": "split pass and combine pass together, per step",
+                         "traffic": NCU_TRAFFIC_BYTES_DECODE.get(w.name)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": DECODE_UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": 2 * args.steps,  # split pass + combine pass per step
+            "launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
+                          "max": max(per_launch_ms)},
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    elif rank == 0:
         peaks, peaks_src = load_peaks()
         flops_step = w.flops
         value = job_tflops(world, flops_step, args.steps, kernel_ms)
@@ -341,7 +436,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=workloads.HEADLINE.name,
-                    choices=[x.name for x in workloads.WORKLOADS])
+                    choices=[x.name for x in workloads.WORKLOADS + workloads.DECODE_WORKLOADS])
     ap.add_argument("--cpu-rows", type=int, default=512,
                     help="query rows per head timed for the CPU baseline")
     ap.add_argument("--ref-rows", type=int, default=64,

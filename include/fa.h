@@ -29,6 +29,8 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -43,7 +45,8 @@ enum fa_status {
   FA_ERR_ALIAS = 6,     /* o or lse overlaps an input, or o overlaps lse */
   FA_ERR_DEVICE = 7,    /* current device is not compute capability 10.3 (sm_103a) */
   FA_ERR_LAUNCH = 8,    /* CUDA runtime / driver error while preparing or launching */
-  FA_ERR_TIMEOUT = 9    /* a kernel wait exceeded its limit (see fa_get_device_status) */
+  FA_ERR_TIMEOUT = 9,   /* a kernel wait exceeded its limit (see fa_get_device_status) */
+  FA_ERR_WORKSPACE = 10 /* split-KV workspace NULL or too small */
 };
 
 /*
@@ -67,6 +70,48 @@ enum fa_status {
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
            int d, int causal, float scale, void *stream);
+
+/*
+ * fa_fwd_splitkv — attention of a short block of queries against a long key
+ * sequence (decode), split over the keys.
+ *
+ * Same operation as fa_fwd with Nq queries and Nk keys; causal masking is
+ * aligned to the end of the keys: query i (0 <= i < Nq) sees keys
+ * 0 .. Nk - Nq + i (for Nq == Nk this is fa_fwd's rule).  The keys are cut
+ * into contiguous ranges, each range's attention (a normalised output and its
+ * log-sum-exp) is computed into `workspace`, and the ranges are merged with
+ * the block-merge identity ("Parsing FlashAttention (2)" eq. (20); "Online
+ * Softmax and FlashAttention", course unit 12):
+ *     LSE = ln sum_s e^(LSE_s),   O = sum_s e^(LSE_s - LSE) O_s.
+ *
+ *   q         : const bf16 [B][H][Nq][d] (device, 16-byte aligned)
+ *   k, v      : const bf16 [B][H][Nk][d] (device, 16-byte aligned)
+ *   o         : bf16 [B][H][Nq][d] (device), written
+ *   lse       : fp32 [B][H][Nq] (device), written (natural log)
+ *   Nq        : 1 .. 16 queries;  Nk >= 1 keys (causal needs Nq <= Nk)
+ *   d         : 64 or 128;  B*H <= 65535
+ *   num_splits: key ranges, 0 = the library's choice for the current device
+ *               (about two CTAs per multiprocessor), else 1 .. 256; the count
+ *               used may be lower (at least 128 keys per range)
+ *   workspace : device scratch of at least fa_fwd_splitkv_workspace_bytes()
+ *               bytes (16-byte aligned), owned by the caller, overwritten;
+ *               must not overlap any other argument.  Calls that share a
+ *               workspace must be ordered (same stream) or they race.
+ * Returns FA_OK or an FA_ERR_* code (FA_ERR_WORKSPACE when the workspace is
+ * missing or too small); validates before enqueueing; asynchronous.
+ */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int Nq, int Nk, int d, int causal, float scale, int num_splits,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_fwd_splitkv needs for these arguments on the current
+ * device (0 on invalid arguments or without a usable device when
+ * num_splits == 0). */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/* Number of key ranges fa_fwd_splitkv uses for these arguments (0 on invalid
+ * arguments or without a usable device when num_splits == 0). */
+int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
 
 /* Human-readable text for a return code (static storage, never NULL). */
 const char *fa_strerror(int code);

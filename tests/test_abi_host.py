@@ -122,3 +122,52 @@ def test_status_hooks_accept_arguments(lib):
     assert lib.fa_set_wait_limit_ns(ctypes.c_ulonglong(0)) == FA_OK
     assert lib.fa_set_fault_injection(0) == FA_OK
     assert lib.fa_get_device_status(None) == FA_ERR_NULL
+
+
+# ---------------------------------------------------------------- split-KV
+
+FA_ERR_WORKSPACE = 10
+
+
+def _split(lib, q=A16, k=2 * A16, v=3 * A16, o=4 * A16, lse=5 * A16, B=1, H=1, Nq=1, Nk=128,
+           d=64, causal=0, scale=0.125, splits=0, ws=6 * A16, ws_bytes=1 << 20):
+    return lib.fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, splits, ws,
+                              ws_bytes, None)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_splitkv_null_pointers_rejected(lib, which):
+    assert _split(lib, **{which: 0}) == FA_ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(Nq=0), dict(Nq=17), dict(Nk=0), dict(B=0),
+                                dict(causal=1, Nq=5, Nk=4), dict(splits=-1), dict(splits=257),
+                                dict(B=256, H=256)])
+def test_splitkv_bad_shapes_rejected(lib, kw):
+    assert _split(lib, **kw) == FA_ERR_SHAPE
+
+
+def test_splitkv_head_dim_alignment_scale(lib):
+    assert _split(lib, d=96) == FA_ERR_HEAD_DIM
+    assert _split(lib, ws=6 * A16 + 8) == FA_ERR_ALIGN
+    assert _split(lib, scale=float("nan")) == FA_ERR_SCALE
+    assert _split(lib, o=A16) == FA_ERR_ALIAS
+
+
+def test_splitkv_workspace_size_formula(lib):
+    # Nk=1000 -> 8 tiles of 128 keys; 4 requested splits -> 2 tiles each.
+    assert lib.fa_fwd_splitkv_num_splits(1, 2, 3, 1000, 64, 4) == 4
+    # partial outputs 4*2*3*64 fp32 = 6144 B, log-sum-exps 24 fp32 -> 256 B (256-byte rounding)
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 2, 3, 1000, 64, 4) == 6144 + 256
+    # more splits than tiles: capped at one tile per split
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 300, 128, 50) == 3
+    assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 17, 300, 128, 2) == 0  # Nq > 16
+
+
+def test_splitkv_without_device_reports_an_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present; covered by the GPU tests")
+    assert _split(lib) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1000, 64, 0) == 0  # needs the device

@@ -18,6 +18,8 @@ from . import _build
 
 __all__ = [
     "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version",
+    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
+    "attention_forward_splitkv",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
     "fa_set_fault_injection", "load_library", "LIB_PATH",
     "FA_DEVICE_STATUS_TIMEOUT", "FA_INJECT_SKIP_FIRST_V_LOAD",
@@ -66,6 +68,13 @@ def load_library(path: str | None = None):
         lib.fa_set_fault_injection.argtypes = [ctypes.c_uint]
         lib.fa_version.restype = i
         lib.fa_version.argtypes = []
+        lib.fa_fwd_splitkv.restype = i
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp,
+                                       ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.fa_fwd_splitkv_num_splits.restype = i
+        lib.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
         _lib = lib
         return lib
 
@@ -143,6 +152,69 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int,
+                                   num_splits: int = 0) -> int:
+    """Workspace bytes fa_fwd_splitkv needs (0 on invalid arguments)."""
+    return int(load_library().fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits))
+
+
+def fa_fwd_splitkv_num_splits(B: int, H: int, Nq: int, Nk: int, d: int,
+                              num_splits: int = 0) -> int:
+    """Key ranges fa_fwd_splitkv uses (0 on invalid arguments)."""
+    return int(load_library().fa_fwd_splitkv_num_splits(B, H, Nq, Nk, d, num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, causal: bool, scale: float, num_splits: int = 0,
+                   workspace=None, stream=None) -> None:
+    """Split-KV attention forward into preallocated CUDA tensors.
+
+    q, o: ``torch.bfloat16`` ``[B, H, Nq, d]`` (Nq <= 16); k, v: ``[B, H, Nk, d]``;
+    lse: ``torch.float32`` ``[B, H, Nq]``.  ``workspace``: a CUDA byte tensor of
+    at least :func:`fa_fwd_splitkv_workspace_bytes`; allocated here when None.
+    """
+    import torch
+
+    B, H, Nq, d = _dims(q)
+    Bk, Hk, Nk, dk = _dims(k)
+    if (Bk, Hk, dk) != (B, H, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q's B, H, d")
+    if tuple(o.shape) != (B, H, Nq, d) or tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("o must be [B, H, Nq, d] and lse [B, H, Nq]")
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor on q's device")
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            nbytes = fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+            if nbytes == 0:
+                raise FAError(2, "fa_fwd_splitkv_workspace_bytes")
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        rc = load_library().fa_fwd_splitkv(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
+            d, int(bool(causal)), float(scale), int(num_splits), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), handle or None)
+        _check(rc, "fa_fwd_splitkv")
+
+
+def attention_forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                              num_splits: int = 0, stream=None):
+    """Allocate O and LSE (and a workspace) and run :func:`fa_fwd_splitkv`."""
+    import torch
+
+    B, H, Nq, d = _dims(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, None, stream)
     return o, lse
 
 

@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_splitkv.cuh"
 
 namespace {
 
@@ -54,6 +55,13 @@ cudaError_t configure_kernel() {
                               static_cast<int>(fa::Cfg<D>::kSmemAlloc));
 }
 
+template <int D>
+cudaError_t configure_split_kernel() {
+  return cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::SplitCfg<D>::kSmemBytes + 128));
+}
+
 // Checks that the current device is sm_103 and configures the kernels for it once.
 int prepare_device(int* dev_out, int* sms_out) {
   int dev = 0;
@@ -78,7 +86,8 @@ int prepare_device(int* dev_out, int* sms_out) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
   if (configure_kernel<64, false>() != cudaSuccess || configure_kernel<64, true>() != cudaSuccess ||
-      configure_kernel<128, false>() != cudaSuccess || configure_kernel<128, true>() != cudaSuccess)
+      configure_kernel<128, false>() != cudaSuccess || configure_kernel<128, true>() != cudaSuccess ||
+      configure_split_kernel<64>() != cudaSuccess || configure_split_kernel<128>() != cudaSuccess)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
   *sms_out = sms;
@@ -181,6 +190,140 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   return neg ? launch<128, true>(mq, mk, mv, prm, sms, s) : launch<128, false>(mq, mk, mv, prm, sms, s);
 }
 
+// ---------------------------------------------------------------- split-KV
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Effective split count and keys per split: the requested count (0 = about
+// two CTAs per multiprocessor), capped by the number of 128-key tiles and by
+// kSplitMaxSplits; every split covers a multiple of 128 keys except the last.
+void split_geometry(int64_t BH, int Nk, int requested, int sms, int* splits, int* keys_per_split) {
+  const int tiles = (Nk + fa::kSplitTileKeys - 1) / fa::kSplitTileKeys;
+  int s = requested;
+  if (s <= 0) s = static_cast<int>((2 * static_cast<int64_t>(sms) + BH - 1) / BH);
+  if (s > tiles) s = tiles;
+  if (s > fa::kSplitMaxSplits) s = fa::kSplitMaxSplits;
+  if (s < 1) s = 1;
+  const int tiles_per_split = (tiles + s - 1) / s;
+  *keys_per_split = tiles_per_split * fa::kSplitTileKeys;
+  *splits = (tiles + tiles_per_split - 1) / tiles_per_split;
+}
+
+size_t split_ws_bytes(int splits, int64_t BH, int Nq, int d) {
+  const size_t rows = static_cast<size_t>(splits) * BH * Nq;
+  return round_up(rows * d * 4, kWsAlign) + round_up(rows * 4, kWsAlign);
+}
+
+int split_shape_ok(int B, int H, int Nq, int Nk, int d, int causal, int num_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  if (Nq > fa::kSplitMaxQ || num_splits < 0 || num_splits > fa::kSplitMaxSplits)
+    return FA_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
+  if (causal && Nq > Nk) return FA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > 65535 || BH * Nk > INT_MAX || BH * Nq > INT_MAX) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+// Split count the library uses for a request on the current device.
+int current_sms() {
+  int dev = 0, sms = 0;
+  if (prepare_device(&dev, &sms) != FA_OK) return 0;
+  return sms;
+}
+
+template <int D>
+int launch_split(const fa::SplitParams& prm, cudaStream_t stream) {
+  const dim3 grid1(static_cast<unsigned>(prm.splits), static_cast<unsigned>(prm.num_bh));
+  fa::fa_splitkv_partial_kernel<D>
+      <<<grid1, fa::kSplitThreads, fa::SplitCfg<D>::kSmemBytes + 128, stream>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  const unsigned rows = static_cast<unsigned>(prm.num_bh * prm.Nq);
+  fa::fa_splitkv_combine_kernel<D><<<(rows + 7) / 8, 256, 0, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (split_shape_ok(B, H, Nq, Nk, d, 0, num_splits) != FA_OK) return 0;
+  const int sms = num_splits > 0 ? 1 : current_sms();
+  if (sms <= 0) return 0;
+  int splits = 0, kps = 0;
+  split_geometry(static_cast<int64_t>(B) * H, Nk, num_splits, sms, &splits, &kps);
+  return splits;
+}
+
+extern "C" size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d,
+                                                 int num_splits) {
+  const int splits = fa_fwd_splitkv_num_splits(B, H, Nq, Nk, d, num_splits);
+  if (splits <= 0) return 0;
+  return split_ws_bytes(splits, static_cast<int64_t>(B) * H, Nq, d);
+}
+
+extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  const int shape = split_shape_ok(B, H, Nq, Nk, d, causal, num_splits);
+  if (shape != FA_OK) return shape;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+       reinterpret_cast<uintptr_t>(workspace)) &
+      15u)
+    return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const size_t q_bytes = static_cast<size_t>(BH) * Nq * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(BH) * Nk * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * Nq * 4;
+  for (const void* in : {q, k, v}) {
+    const size_t n = (in == q) ? q_bytes : kv_bytes;
+    if (overlaps(o, q_bytes, in, n) || overlaps(lse, lse_bytes, in, n)) return FA_ERR_ALIAS;
+  }
+  if (overlaps(o, q_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
+  if (prep != FA_OK) return prep;
+  int splits = 0, kps = 0;
+  split_geometry(BH, Nk, num_splits, sms, &splits, &kps);
+  const size_t need = split_ws_bytes(splits, BH, Nq, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  for (const void* other : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)}) {
+    const size_t n = other == q || other == o ? q_bytes : other == lse ? lse_bytes : kv_bytes;
+    if (overlaps(workspace, need, other, n)) return FA_ERR_ALIAS;
+  }
+
+  fa::SplitParams prm;
+  prm.q = static_cast<const uint16_t*>(q);
+  prm.k = static_cast<const uint16_t*>(k);
+  prm.v = static_cast<const uint16_t*>(v);
+  prm.o = static_cast<uint16_t*>(o);
+  prm.lse = lse;
+  const size_t rows = static_cast<size_t>(splits) * BH * Nq;
+  prm.ws_o = static_cast<float*>(workspace);
+  prm.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        round_up(rows * d * 4, kWsAlign));
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.num_bh = static_cast<int>(BH);
+  prm.splits = splits;
+  prm.keys_per_split = kps;
+  prm.causal = causal;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_split<64>(prm, s) : launch_split<128>(prm, s);
+}
+
 extern "C" const char* fa_strerror(int code) {
   switch (code) {
     case FA_OK: return "success";
@@ -193,6 +336,7 @@ extern "C" const char* fa_strerror(int code) {
     case FA_ERR_DEVICE: return "current device is not sm_103 (GB300)";
     case FA_ERR_LAUNCH: return "CUDA error while preparing or launching the kernel";
     case FA_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
+    case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_fwd_splitkv_workspace_bytes()";
     default: return "unknown error code";
   }
 }

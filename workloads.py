@@ -67,11 +67,60 @@ HEADLINE = WORKLOADS[2]
 RAGGED_N = (1, 17, 127, 129, 1000, 4097)
 
 
-def by_name(name: str) -> Workload:
-    for w in WORKLOADS:
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """A short block of queries against a long key sequence (split-KV path).
+    Causal masking, when set, is aligned to the end of the keys."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    scale: float
+    seed: int = 0
+
+    @property
+    def flops(self) -> float:
+        """4·B·H·Nq·Nk·d (the same count as the square workloads, unmasked)."""
+        return 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+
+    @property
+    def io_bytes(self) -> int:
+        """Algorithmic HBM bytes: read Q, K, V once (bf16), write O (bf16)
+        and LSE (fp32) once."""
+        bh = self.B * self.H
+        return bh * (2 * self.Nq * self.d * 2 + 2 * self.Nk * self.d * 2 + self.Nq * 4)
+
+
+# Decode: one (and sixteen) new queries per head against a 16384-key cache;
+# K and V (268 MB) exceed L2, so the path is bound by HBM.
+DECODE_WORKLOADS = (
+    DecodeWorkload("decode_b4h16q1k16384d128", 4, 16, 1, 16384, 128, False,
+                   1.0 / math.sqrt(128), seed=5),
+    DecodeWorkload("decode_b4h16q16k16384d128_causal", 4, 16, 16, 16384, 128, True,
+                   1.0 / math.sqrt(128), seed=6),
+)
+
+
+def by_name(name: str):
+    for w in WORKLOADS + DECODE_WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)
+
+
+def generate_decode(w: DecodeWorkload):
+    """Return ``(q [B,H,Nq,d], k [B,H,Nk,d], v [B,H,Nk,d])`` as uint16 bf16
+    bit patterns: one PCG64(seed) stream draws q, then k, then v (fp32
+    standard normal, rounded to bf16)."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    out = []
+    for n in (w.Nq, w.Nk, w.Nk):
+        x = rng.standard_normal(size=(w.B, w.H, n, w.d), dtype=np.float32)
+        out.append(f32_to_bf16_bits(x))
+    return tuple(out)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
