@@ -155,12 +155,14 @@ def test_splitkv_head_dim_alignment_scale(lib):
 
 
 def test_splitkv_workspace_size_formula(lib):
-    # Nk=1000 -> 8 tiles of 128 keys; 4 requested splits -> 2 tiles each.
+    # Nk=1000 -> 16 tiles of 64 keys; 4 requested splits -> 4 tiles each.
     assert lib.fa_fwd_splitkv_num_splits(1, 2, 3, 1000, 64, 4) == 4
+    # 7 requested -> 3 tiles per split -> 6 ranges cover the 16 tiles
+    assert lib.fa_fwd_splitkv_num_splits(1, 2, 3, 1000, 64, 7) == 6
     # partial outputs 4*2*3*64 fp32 = 6144 B, log-sum-exps 24 fp32 -> 256 B (256-byte rounding)
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 2, 3, 1000, 64, 4) == 6144 + 256
     # more splits than tiles: capped at one tile per split
-    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 300, 128, 50) == 3
+    assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 300, 128, 50) == 5
     assert lib.fa_fwd_splitkv_workspace_bytes(1, 1, 17, 300, 128, 2) == 0  # Nq > 16
 
 

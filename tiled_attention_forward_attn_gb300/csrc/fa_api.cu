@@ -59,7 +59,7 @@ template <int D>
 cudaError_t configure_split_kernel() {
   return cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(fa::SplitCfg<D>::kSmemBytes + 128));
+                              static_cast<int>(fa::SplitCfg<D>::kSmemAlloc));
 }
 
 // Checks that the current device is sm_103 and configures the kernels for it once.
@@ -96,13 +96,13 @@ int prepare_device(int* dev_out, int* sms_out) {
 }
 
 // [BH][N][d] bf16 viewed as a 3-D tensor (d innermost), boxes of
-// 64 columns x 128 rows x 1 slice with the 128-byte swizzle.
-bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+// 64 columns x `box_rows` rows x 1 slice with the 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUresult r =
       g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
@@ -198,13 +198,17 @@ constexpr size_t kWsAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Effective split count and keys per split: the requested count (0 = about
-// two CTAs per multiprocessor), capped by the number of 128-key tiles and by
-// kSplitMaxSplits; every split covers a multiple of 128 keys except the last.
+// Effective split count and keys per split: the requested count, or (0) the
+// largest count whose CTAs all fit in one wave (kSplitCtasPerSm per
+// multiprocessor), at least 1; capped by the number of 64-key tiles and by
+// kSplitMaxSplits.  Every split covers a multiple of 64 keys except the last.
 void split_geometry(int64_t BH, int Nk, int requested, int sms, int* splits, int* keys_per_split) {
   const int tiles = (Nk + fa::kSplitTileKeys - 1) / fa::kSplitTileKeys;
   int s = requested;
-  if (s <= 0) s = static_cast<int>((2 * static_cast<int64_t>(sms) + BH - 1) / BH);
+  if (s <= 0) {
+    const int64_t slots = static_cast<int64_t>(fa::kSplitCtasPerSm) * sms;
+    s = static_cast<int>(slots / BH < fa::kSplitMaxSplits ? slots / BH : fa::kSplitMaxSplits);
+  }
   if (s > tiles) s = tiles;
   if (s > fa::kSplitMaxSplits) s = fa::kSplitMaxSplits;
   if (s < 1) s = 1;
@@ -238,10 +242,11 @@ int current_sms() {
 }
 
 template <int D>
-int launch_split(const fa::SplitParams& prm, cudaStream_t stream) {
+int launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const fa::SplitParams& prm,
+                 cudaStream_t stream) {
   const dim3 grid1(static_cast<unsigned>(prm.splits), static_cast<unsigned>(prm.num_bh));
   fa::fa_splitkv_partial_kernel<D>
-      <<<grid1, fa::kSplitThreads, fa::SplitCfg<D>::kSmemBytes + 128, stream>>>(prm);
+      <<<grid1, fa::kSplitThreads, fa::SplitCfg<D>::kSmemAlloc, stream>>>(mk, mv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   const unsigned rows = static_cast<unsigned>(prm.num_bh * prm.Nq);
   fa::fa_splitkv_combine_kernel<D><<<(rows + 7) / 8, 256, 0, stream>>>(prm);
@@ -302,10 +307,15 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
     if (overlaps(workspace, need, other, n)) return FA_ERR_ALIAS;
   }
 
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return FA_ERR_LAUNCH;
+  CUtensorMap mk, mv;
+  if (!encode_map(&mk, k, static_cast<int>(BH), Nk, d, fa::kSplitTileKeys) ||
+      !encode_map(&mv, v, static_cast<int>(BH), Nk, d, fa::kSplitTileKeys))
+    return FA_ERR_LAUNCH;
+
   fa::SplitParams prm;
   prm.q = static_cast<const uint16_t*>(q);
-  prm.k = static_cast<const uint16_t*>(k);
-  prm.v = static_cast<const uint16_t*>(v);
   prm.o = static_cast<uint16_t*>(o);
   prm.lse = lse;
   const size_t rows = static_cast<size_t>(splits) * BH * Nq;
@@ -321,7 +331,7 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_split<64>(prm, s) : launch_split<128>(prm, s);
+  return d == 64 ? launch_split<64>(mk, mv, prm, s) : launch_split<128>(mk, mv, prm, s);
 }
 
 extern "C" const char* fa_strerror(int code) {

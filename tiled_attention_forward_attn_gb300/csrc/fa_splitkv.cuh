@@ -11,19 +11,22 @@
 // a range with no visible key (LSE_s = -inf) weighing 0.  Causal masking is
 // aligned to the end of the keys: query i sees keys 0 .. Nk - Nq + i.
 //
-// With a handful of queries the work is bound by reading K and V from HBM
-// (about one FLOP per byte), so pass 1 runs on the CUDA cores: a producer warp
-// streams 128-key K and V tiles (contiguous rows) into a shared-memory ring
-// with 1-D bulk copies, and eight consumer warps each own 16 keys of every
-// tile: a lane pair computes one q.k dot product (half of d each), the warp
-// keeps a running max / exponent sum / output slice per query (lane l owns
-// output columns [D/32*l, D/32*(l+1))), and at the end the eight warp states
-// are merged in shared memory.  Shared-memory reads are skewed per lane so
-// the 32 lanes of a warp never queue on one bank.
+// With at most 16 queries the work is bound by reading K and V from HBM
+// (Nq FLOPs per byte of K and V).  Pass 1: a
+// producer warp streams 64-key K and V tiles into a shared-memory ring with
+// TMA (128-byte swizzle, evict-first L2 hint, zero fill past the end), and
+// four consumer warps each take 16 keys of every tile: S = Q K^T with
+// warp-level 16x8x16 tensor-core MMAs (the query block is exactly one
+// 16-row MMA tile), the online-softmax update in registers, and O += P V
+// with P kept in registers as the next MMA's A operand.  At the end of the
+// range the four warp states are merged in shared memory.  Two CTAs fit on
+// a multiprocessor; the host picks the split count so that all CTAs run in
+// one wave when the batch allows.
 //
 // Waits are bounded like those of the main kernel (status word, no hang).
 #pragma once
 
+#include <climits>
 #include <cstdint>
 #include <cuda.h>
 #include <math_constants.h>
@@ -33,17 +36,15 @@
 
 namespace fa {
 
-constexpr int kSplitMaxQ = 16;          // queries per call
-constexpr int kSplitTileKeys = 128;     // keys per streamed tile
-constexpr int kSplitConsumerWarps = 8;  // 16 keys of each tile per warp
+constexpr int kSplitMaxQ = 16;          // queries per call (one MMA row tile)
+constexpr int kSplitTileKeys = 64;      // keys per streamed tile
+constexpr int kSplitConsumerWarps = 4;  // 16 keys of each tile per warp
 constexpr int kSplitThreads = (kSplitConsumerWarps + 1) * 32;
-constexpr int kSplitStages = 2;
+constexpr int kSplitCtasPerSm = 2;
 constexpr int kSplitMaxSplits = 256;
 
 struct SplitParams {
   const uint16_t* q;  // [BH][Nq][D] bf16
-  const uint16_t* k;  // [BH][Nk][D]
-  const uint16_t* v;  // [BH][Nk][D]
   uint16_t* o;        // [BH][Nq][D] bf16 (pass 2)
   float* lse;         // [BH][Nq] (pass 2)
   float* ws_o;        // [splits][BH][Nq][D] fp32 partial outputs
@@ -55,28 +56,18 @@ struct SplitParams {
 
 template <int D>
 struct SplitCfg {
-  static constexpr uint32_t kTileBytes = kSplitTileKeys * D * 2;  // K (or V) tile
-  static constexpr uint32_t kOffK = 0;
-  static constexpr uint32_t kOffV = kOffK + kSplitStages * kTileBytes;
-  static constexpr uint32_t kOffQ = kOffV + kSplitStages * kTileBytes;  // bf16 [16][D]
-  // Per-warp running state of every query: max m and exponent sum l
-  // [warps][16] and the unnormalised output O [warps][16][D], fp32.
-  static constexpr uint32_t kOffM = kOffQ + kSplitMaxQ * D * 2;
-  static constexpr uint32_t kOffL = kOffM + kSplitConsumerWarps * kSplitMaxQ * 4;
-  static constexpr uint32_t kOffAcc = kOffL + kSplitConsumerWarps * kSplitMaxQ * 4;
-  static constexpr uint32_t kOffBar = kOffAcc + kSplitConsumerWarps * kSplitMaxQ * D * 4;
-  static constexpr uint32_t kSmemBytes = kOffBar + 2 * kSplitStages * 8 + 16;
-  static_assert(kSmemBytes + 128 <= 232448, "dynamic shared memory per block");
+  static constexpr int kStages = D == 64 ? 6 : 3;
+  static constexpr uint32_t kBoxBytes = kSplitTileKeys * 128;    // 64 keys x 64 columns
+  static constexpr uint32_t kTileBytes = kSplitTileKeys * D * 2;  // K (or V) tile: D/64 boxes
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes;         // K then V
+  static constexpr uint32_t kOffBar = kStages * kStageBytes;
+  // The warp merge reuses the ring: O [warps][16][D], then m and l [warps][16].
+  static constexpr uint32_t kMergeBytes = kSplitConsumerWarps * kSplitMaxQ * (D + 2) * 4;
+  static_assert(kMergeBytes <= kOffBar, "merge area fits in the ring");
+  static constexpr uint32_t kSmemBytes = kOffBar + 2 * kStages * 8;
+  static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // 1024-byte alignment for SW128
+  static_assert(kSplitCtasPerSm * (kSmemAlloc + 1024) <= 233472, "two CTAs per multiprocessor");
 };
-
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // Bounded wait (same contract as the main kernel's): false on expiry, after
 // recording FA_DEVICE_STATUS_TIMEOUT.
@@ -91,22 +82,28 @@ __device__ __forceinline__ bool split_wait(uint32_t bar, uint32_t parity, uint64
   return false;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Byte offset of 16-byte chunk `chunk` (8 columns) of row `row` in a tile of
+// D/64 boxes, each 64 rows x 128 bytes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * (kSplitTileKeys * 128) + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
 
 // Pass 1: one CTA per (split, batch*head).
 template <int D>
-__global__ void __launch_bounds__(kSplitThreads, 1)
-    fa_splitkv_partial_kernel(const SplitParams p) {
+__global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
+    fa_splitkv_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
+                              const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
   using C = SplitCfg<D>;
-  constexpr int kCols = D / 32;             // output columns per lane
-  constexpr int kChunksHalf = D / 16;       // 16-byte chunks in half a row
+  constexpr int kS = C::kStages;
+  constexpr int kKSteps = D / 16;  // MMA k-steps of Q K^T over the head dimension
+  constexpr int kNTiles = D / 8;   // 8-column MMA tiles of the output
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                             ~static_cast<uintptr_t>(127));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::kOffBar;
-  const uint32_t bar_empty = bar_full + 8 * kSplitStages;
+  const uint32_t bar_empty = bar_full + 8 * kS;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int split = blockIdx.x;
@@ -116,169 +113,196 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   const int k_end = min(p.Nk, k_begin + p.keys_per_split);
   const int n_tiles = k_end > k_begin ? (k_end - k_begin + kSplitTileKeys - 1) / kSplitTileKeys : 0;
 
-  // Q -> shared memory (bf16), all threads.
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(bh) * Nq * D);
-    uint4* dst = reinterpret_cast<uint4*>(smem + C::kOffQ);
-    for (int i = threadIdx.x; i < Nq * D / 8; i += blockDim.x) dst[i] = src[i];
-  }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSplitStages; ++s) {
+    for (int s = 0; s < kS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kSplitConsumerWarps);
     }
     fence_barrier_init();
   }
+  if (threadIdx.x == 32 * kSplitConsumerWarps) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
   __syncthreads();
 
-  // Consumer state in shared memory: m, l per (warp, query) and this
-  // lane's D/32 output columns per (warp, query).
-  const float c = p.scale_log2;
-  float* m_s = reinterpret_cast<float*>(smem + C::kOffM);
-  float* l_s = reinterpret_cast<float*>(smem + C::kOffL);
-  float* acc_s = reinterpret_cast<float*>(smem + C::kOffAcc);
-  if (warp < kSplitConsumerWarps) {
-    if (lane < kSplitMaxQ) {
-      m_s[warp * kSplitMaxQ + lane] = -CUDART_INF_F;
-      l_s[warp * kSplitMaxQ + lane] = 0.0f;
-    }
-    for (int i = 0; i < kSplitMaxQ; ++i)
-#pragma unroll
-      for (int e = 0; e < kCols; ++e) acc_s[(warp * kSplitMaxQ + i) * D + lane * kCols + e] = 0.0f;
-    __syncwarp();
-  }
   bool ok = true;
+  // Consumer state (rows g and g + 8 of the 16-row query block).
+  const int g = lane >> 2, t4 = lane & 3;
+  float acc[kNTiles][4];
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+  for (int n = 0; n < kNTiles; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
 
   if (warp == kSplitConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint16_t* kb = p.k + static_cast<size_t>(bh) * p.Nk * D;
-      const uint16_t* vb = p.v + static_cast<size_t>(bh) * p.Nk * D;
+      const uint64_t policy = make_l2_policy_evict_first();
       int issued = 0;
       for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % kSplitStages;
-        if (t >= kSplitStages &&
-            !split_wait(bar_empty + 8 * s, static_cast<uint32_t>(t / kSplitStages - 1) & 1u,
-                        p.wait_limit_ns))
+        const int s = t % kS;
+        if (t >= kS &&
+            !split_wait(bar_empty + 8 * s, static_cast<uint32_t>(t / kS - 1) & 1u, p.wait_limit_ns))
           break;
         const int k0 = k_begin + t * kSplitTileKeys;
-        const int rows = min(kSplitTileKeys, k_end - k0);
-        const uint32_t bytes = static_cast<uint32_t>(rows) * D * 2;
-        mbar_arrive_expect_tx(bar_full + 8 * s, 2 * bytes);
-        bulk_copy_g2s(sbase + C::kOffK + s * C::kTileBytes, kb + static_cast<size_t>(k0) * D, bytes,
-                      bar_full + 8 * s);
-        bulk_copy_g2s(sbase + C::kOffV + s * C::kTileBytes, vb + static_cast<size_t>(k0) * D, bytes,
-                      bar_full + 8 * s);
+        const uint32_t stage = sbase + s * C::kStageBytes;
+        mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_3d_hint(stage + b * C::kBoxBytes, &tm_k, bar_full + 8 * s, 64 * b, k0, bh, policy);
+          tma_load_3d_hint(stage + C::kTileBytes + b * C::kBoxBytes, &tm_v, bar_full + 8 * s, 64 * b,
+                           k0, bh, policy);
+        }
         issued = t + 1;
       }
-      // Drain: the last copy into each stage must land before the CTA exits.
-      for (int s = 0; s < kSplitStages; ++s) {
+      // Drain: the last copy into each stage must land before the CTA exits
+      // or the ring is reused by the merge.
+      for (int s = 0; s < kS; ++s) {
         if (issued > s) {
-          const int last = issued - 1 - ((issued - 1 - s) % kSplitStages);
-          split_wait(bar_full + 8 * s, static_cast<uint32_t>(last / kSplitStages) & 1u,
-                     p.wait_limit_ns);
+          const int last = issued - 1 - ((issued - 1 - s) % kS);
+          split_wait(bar_full + 8 * s, static_cast<uint32_t>(last / kS) & 1u, p.wait_limit_ns);
         }
       }
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int key_in_tile = 16 * warp + (lane >> 1);
-    const int half = lane & 1;
-    const uint8_t* q_s = smem + C::kOffQ;
+    // Q as MMA A fragments, loaded once; rows past Nq are zero.
+    uint32_t qa[kKSteps][4];
+    {
+      const uint32_t* qg = reinterpret_cast<const uint32_t*>(p.q + static_cast<size_t>(bh) * Nq * D);
+#pragma unroll
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        const int c0 = 16 * ks + 2 * t4;
+        qa[ks][0] = g < Nq ? qg[(g * D + c0) >> 1] : 0u;
+        qa[ks][1] = g + 8 < Nq ? qg[((g + 8) * D + c0) >> 1] : 0u;
+        qa[ks][2] = g < Nq ? qg[(g * D + c0 + 8) >> 1] : 0u;
+        qa[ks][3] = g + 8 < Nq ? qg[((g + 8) * D + c0 + 8) >> 1] : 0u;
+      }
+    }
+    const float c = p.scale_log2;
+    // Last key each of the two rows may see (end-aligned causal mask).
+    const int lim0 = p.causal ? p.Nk - Nq + g : INT_MAX;
+    const int lim1 = p.causal ? p.Nk - Nq + g + 8 : INT_MAX;
+    // ldmatrix row addresses: lane l feeds row (l & 7) of matrix (l >> 3).
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int k_row = 16 * warp + ((mi >> 1) << 3) + r8;  // K: matrices (keys 0-7|8-15) x (cols lo|hi)
+    const int v_row = 16 * warp + ((mi & 1) << 3) + r8;   // V: matrices (keys lo|hi) x (n | n+1)
+
     for (int t = 0; t < n_tiles; ++t) {
-      const int s = t % kSplitStages;
-      const bool got = split_wait(bar_full + 8 * s, static_cast<uint32_t>(t / kSplitStages) & 1u,
+      const int s = t % kS;
+      const bool got = split_wait(bar_full + 8 * s, static_cast<uint32_t>(t / kS) & 1u,
                                   p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
-      const uint8_t* k_s = smem + C::kOffK + s * C::kTileBytes;
-      const uint8_t* v_s = smem + C::kOffV + s * C::kTileBytes;
-      const int k0 = k_begin + t * kSplitTileKeys;
-      const int key = k0 + key_in_tile;
-      const bool in_range = key < k_end;
-      // This lane's half row of K, read in a lane-skewed chunk order.
-      const uint8_t* k_row = k_s + key_in_tile * (D * 2) + half * D;
-#pragma unroll 1
-      for (int i = 0; i < Nq; ++i) {
-        const uint8_t* q_row = q_s + i * (D * 2) + half * D;
-        float dot = 0.0f;
+      const uint32_t kt = sbase + s * C::kStageBytes;
+      const uint32_t vt = kt + C::kTileBytes;
+
+      // S (16 queries x this warp's 16 keys) = Q K^T.
+      float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-        for (int cc = 0; cc < kChunksHalf; ++cc) {
-          const int ch = (cc + (lane >> 1)) % kChunksHalf;
-          const uint4 kv = *reinterpret_cast<const uint4*>(k_row + ch * 16);
-          const uint4 qv = *reinterpret_cast<const uint4*>(q_row + ch * 16);
-          dot = fmaf(bf16_lo(qv.x), bf16_lo(kv.x), dot);
-          dot = fmaf(bf16_hi(qv.x), bf16_hi(kv.x), dot);
-          dot = fmaf(bf16_lo(qv.y), bf16_lo(kv.y), dot);
-          dot = fmaf(bf16_hi(qv.y), bf16_hi(kv.y), dot);
-          dot = fmaf(bf16_lo(qv.z), bf16_lo(kv.z), dot);
-          dot = fmaf(bf16_hi(qv.z), bf16_hi(kv.z), dot);
-          dot = fmaf(bf16_lo(qv.w), bf16_lo(kv.w), dot);
-          dot = fmaf(bf16_hi(qv.w), bf16_hi(kv.w), dot);
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        uint32_t b[4];
+        ldsm_x4(b, kt + sw128_offset(k_row, 2 * ks + (mi & 1)));
+        mma_bf16_16816(sc[0], qa[ks], b[0], b[1]);
+        mma_bf16_16816(sc[1], qa[ks], b[2], b[3]);
+      }
+
+      // Mask, running max, probabilities.  Keys past the range's end are
+      // masked (TMA filled them with zeros or the next range's rows).
+      const int key0 = k_begin + t * kSplitTileKeys + 16 * warp + 2 * t4;
+      float x0[4], x1[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = key0 + 8 * j + e;
+          const bool in = key < k_end;
+          x0[2 * j + e] = (in && key <= lim0) ? sc[j][e] * c : -CUDART_INF_F;
+          x1[2 * j + e] = (in && key <= lim1) ? sc[j][2 + e] * c : -CUDART_INF_F;
         }
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);  // the other half of the row
-        const bool visible = in_range && (!p.causal || key <= p.Nk - Nq + i);
-        const float x = visible ? dot * c : -CUDART_INF_F;
-        // Max over the warp's 16 keys (lane pairs hold the same value).
-        float mt = x;
+      float mx0 = fmaxf(fmaxf(x0[0], x0[1]), fmaxf(x0[2], x0[3]));
+      float mx1 = fmaxf(fmaxf(x1[0], x1[1]), fmaxf(x1[2], x1[3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // Base 0 while a row has seen no visible key: its probabilities and
+      // rescale factors are then exactly 0 (no -inf - -inf).
+      const float mu0 = mn0 == -CUDART_INF_F ? 0.0f : mn0;
+      const float mu1 = mn1 == -CUDART_INF_F ? 0.0f : mn1;
+      const float alpha0 = ex2_approx(m0 - mu0), alpha1 = ex2_approx(m1 - mu1);
+      m0 = mn0;
+      m1 = mn1;
+      float p0[4], p1[4];
 #pragma unroll
-        for (int off = 2; off < 32; off <<= 1)
-          mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-        const float m_old = m_s[warp * kSplitMaxQ + i];
-        const float m_new = fmaxf(m_old, mt);
-        if (m_new == -CUDART_INF_F) continue;  // nothing visible to this warp yet (uniform)
-        const float alpha = ex2_approx(m_old - m_new);  // 0 when m_old was -inf
-        const float pr = ex2_approx(x - m_new);         // 0 for masked keys
-        float ps = half == 0 ? pr : 0.0f;               // count each key once
+      for (int e = 0; e < 4; ++e) {
+        p0[e] = ex2_approx(x0[e] - mu0);
+        p1[e] = ex2_approx(x1[e] - mu1);
+      }
+      l0 = l0 * alpha0 + ((p0[0] + p0[1]) + (p0[2] + p0[3]));
+      l1 = l1 * alpha1 + ((p1[0] + p1[1]) + (p1[2] + p1[3]));
+      // P as the A operand of the 16-key step: the S accumulator layout of
+      // key tiles 0 and 1 is the A layout of keys 0-15.
+      const uint32_t pa[4] = {pack_bf16x2(p0[0], p0[1]), pack_bf16x2(p1[0], p1[1]),
+                              pack_bf16x2(p0[2], p0[3]), pack_bf16x2(p1[2], p1[3])};
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-        const float l_new = l_s[warp * kSplitMaxQ + i] * alpha + ps;
-        __syncwarp();
-        if (lane == 0) {
-          m_s[warp * kSplitMaxQ + i] = m_new;
-          l_s[warp * kSplitMaxQ + i] = l_new;
-        }
-        float* acc_row = acc_s + (warp * kSplitMaxQ + i) * D + lane * kCols;
-        float acc[kCols];
-#pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] = acc_row[e] * alpha;
-        // Output slice += sum over the warp's 16 keys of p_key * V[key][lane's columns].
-        // Rows past the end of the range were not copied this time (stale or
-        // never written), so they are skipped rather than multiplied by 0.
-        const int warp_keys = k_end - (k0 + 16 * warp);  // uniform across the warp
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          if (kk >= warp_keys) break;
-          const float pk = __shfl_sync(0xffffffffu, pr, 2 * kk);
-          const uint8_t* v_row = v_s + (16 * warp + kk) * (D * 2) + lane * (kCols * 2);
-          if (kCols == 4) {
-            const uint2 vv = *reinterpret_cast<const uint2*>(v_row);
-            acc[0] = fmaf(pk, bf16_lo(vv.x), acc[0]);
-            acc[1] = fmaf(pk, bf16_hi(vv.x), acc[1]);
-            acc[2] = fmaf(pk, bf16_lo(vv.y), acc[2]);
-            acc[3] = fmaf(pk, bf16_hi(vv.y), acc[3]);
-          } else {
-            const uint32_t vv = *reinterpret_cast<const uint32_t*>(v_row);
-            acc[0] = fmaf(pk, bf16_lo(vv), acc[0]);
-            acc[1] = fmaf(pk, bf16_hi(vv), acc[1]);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < kCols; ++e) acc_row[e] = acc[e];
-        __syncwarp();
+      for (int n = 0; n < kNTiles; n += 2) {
+        uint32_t b[4];
+        ldsm_x4_trans(b, vt + sw128_offset(v_row, n + (mi >> 1)));
+        acc[n][0] *= alpha0;
+        acc[n][1] *= alpha0;
+        acc[n][2] *= alpha1;
+        acc[n][3] *= alpha1;
+        acc[n + 1][0] *= alpha0;
+        acc[n + 1][1] *= alpha0;
+        acc[n + 1][2] *= alpha1;
+        acc[n + 1][3] *= alpha1;
+        mma_bf16_16816(acc[n], pa, b[0], b[1]);
+        mma_bf16_16816(acc[n + 1], pa, b[2], b[3]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
+    // Row sums: each lane of a quad summed a quarter of the keys.
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   }
 
   // ------------------------------------------------------------ merge warps
-  float* ms = m_s;
-  float* ls = l_s;
-  float* os = acc_s;
   const bool all_ok = __syncthreads_and(ok);
+  const size_t row_base = (static_cast<size_t>(split) * p.num_bh + bh) * Nq;
+  if (!all_ok) {
+    for (int idx = threadIdx.x; idx < Nq * D; idx += kSplitThreads) {
+      p.ws_o[row_base * D + idx] = 0.0f;
+      if (idx % D == 0) p.ws_lse[row_base + idx / D] = -CUDART_INF_F;
+    }
+    return;
+  }
+  // Every issued tile was consumed, so no copy is in flight: reuse the ring.
+  float* os = reinterpret_cast<float*>(smem);                           // [warp][16][D]
+  float* ms = os + kSplitConsumerWarps * kSplitMaxQ * D;                // [warp][16]
+  float* ls = ms + kSplitConsumerWarps * kSplitMaxQ;                    // [warp][16]
+  if (warp < kSplitConsumerWarps) {
+#pragma unroll
+    for (int n = 0; n < kNTiles; ++n) {
+      float* r0 = os + (warp * kSplitMaxQ + g) * D + 8 * n + 2 * t4;
+      float* r1 = r0 + 8 * D;
+      *reinterpret_cast<float2*>(r0) = make_float2(acc[n][0], acc[n][1]);
+      *reinterpret_cast<float2*>(r1) = make_float2(acc[n][2], acc[n][3]);
+    }
+    if (t4 == 0) {
+      ms[warp * kSplitMaxQ + g] = m0;
+      ms[warp * kSplitMaxQ + g + 8] = m1;
+      ls[warp * kSplitMaxQ + g] = l0;
+      ls[warp * kSplitMaxQ + g + 8] = l1;
+    }
+  }
+  __syncthreads();
   // One thread per (query, column): merge the warps, normalise, write.
   for (int idx = threadIdx.x; idx < Nq * D; idx += kSplitThreads) {
     const int i = idx / D;
@@ -296,10 +320,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         o += e * os[(w * kSplitMaxQ + i) * D + col];
       }
     }
-    const size_t row = (static_cast<size_t>(split) * p.num_bh + bh) * Nq + i;
-    const bool any = all_ok && l > 0.0f;
-    p.ws_o[row * D + col] = any ? o / l : 0.0f;
-    if (col == 0) p.ws_lse[row] = any ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+    const bool any = l > 0.0f;
+    p.ws_o[(row_base + i) * D + col] = any ? o / l : 0.0f;
+    if (col == 0) p.ws_lse[row_base + i] = any ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
   }
 }
 
