@@ -91,8 +91,9 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
  *   Nq        : 1 .. 16 queries;  Nk >= 1 keys (causal needs Nq <= Nk)
  *   d         : 64 or 128;  B*H <= 65535
  *   num_splits: key ranges, 0 = the library's choice for the current device
- *               (about two CTAs per multiprocessor), else 1 .. 256; the count
- *               used may be lower (at least 128 keys per range)
+ *               (the most ranges whose CTAs, two per multiprocessor, all run
+ *               at once), else 1 .. 256; the count used may be lower (at
+ *               least 64 keys per range)
  *   workspace : device scratch of at least fa_fwd_splitkv_workspace_bytes()
  *               bytes (16-byte aligned), owned by the caller, overwritten;
  *               must not overlap any other argument.  Calls that share a
