@@ -46,7 +46,8 @@ enum fa_status {
   FA_ERR_DEVICE = 7,    /* current device is not compute capability 10.3 (sm_103a) */
   FA_ERR_LAUNCH = 8,    /* CUDA runtime / driver error while preparing or launching */
   FA_ERR_TIMEOUT = 9,   /* a kernel wait exceeded its limit (see fa_get_device_status) */
-  FA_ERR_WORKSPACE = 10 /* split-KV workspace NULL or too small */
+  FA_ERR_WORKSPACE = 10, /* split-KV workspace NULL or too small */
+  FA_ERR_SCRATCH_LIMIT = 11 /* fa_fwd_splitkv_static: request exceeds its built-in scratch */
 };
 
 /*
@@ -113,6 +114,42 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n
 /* Number of key ranges fa_fwd_splitkv uses for these arguments (0 on invalid
  * arguments or without a usable device when num_splits == 0). */
 int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * fa_fwd_splitkv_static — fa_fwd_splitkv for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a library service.
+ *
+ * Some callers cannot call cudaMalloc or any allocator: code whose device
+ * memory all belongs to a pool or arena it does not control, code that must
+ * not risk the implicit synchronisation or the failure of an allocation in
+ * the middle of its work, and plug-ins whose host hands them no allocator.
+ * This entry point takes the same inputs and outputs as fa_fwd_splitkv but
+ * no workspace: its scratch (the per-range partial outputs and
+ * log-sum-exps) lives in a device array built into the library, of
+ * fa_fwd_splitkv_static_scratch_bytes() bytes (8 MiB), which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *
+ * Arguments, layout, results and arithmetic are those of fa_fwd_splitkv
+ * (num_splits included), without workspace and workspace_bytes.  A request
+ * whose scratch would exceed the array (about splits * B * H * Nq * (4d + 4)
+ * bytes; fa_fwd_splitkv_workspace_bytes() gives the exact figure) is
+ * rejected with FA_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array, which keeps the
+ * last call's contents (nothing in it needs to start at zero); calls whose
+ * kernels overlap on the GPU, e.g. on two unordered streams or from two
+ * host threads, race on it and give undefined results: order them on one
+ * stream.  Returns FA_OK or an FA_ERR_* code; asynchronous.
+ */
+int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int H, int Nq, int Nk, int d, int causal, float scale, int num_splits,
+                          void *stream);
+
+/* Size in bytes of fa_fwd_splitkv_static's built-in scratch array. */
+size_t fa_fwd_splitkv_static_scratch_bytes(void);
 
 /* Human-readable text for a return code (static storage, never NULL). */
 const char *fa_strerror(int code);

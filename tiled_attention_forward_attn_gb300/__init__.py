@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
-    "attention_forward_splitkv",
+    "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
     "fa_set_fault_injection", "load_library", "LIB_PATH",
     "FA_DEVICE_STATUS_TIMEOUT", "FA_INJECT_SKIP_FIRST_V_LOAD",
@@ -75,6 +75,10 @@ def load_library(path: str | None = None):
         lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.fa_fwd_splitkv_num_splits.restype = i
         lib.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
+        lib.fa_fwd_splitkv_static.restype = i
+        lib.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_splitkv_static_scratch_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_splitkv_static_scratch_bytes.argtypes = []
         _lib = lib
         return lib
 
@@ -216,6 +220,41 @@ def attention_forward_splitkv(q, k, v, causal: bool = False, scale: float | None
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, None, stream)
     return o, lse
+
+
+def fa_fwd_splitkv_static_scratch_bytes() -> int:
+    """Size of the scratch array built into the library for
+    :func:`fa_fwd_splitkv_static`."""
+    return int(load_library().fa_fwd_splitkv_static_scratch_bytes())
+
+
+def fa_fwd_splitkv_static(q, k, v, o, lse, causal: bool, scale: float, num_splits: int = 0,
+                          stream=None) -> None:
+    """:func:`fa_fwd_splitkv` without a workspace and without any device
+    allocation, for callers that cannot allocate: the scratch is the
+    library's built-in array (shared by every call on a device; order calls
+    on one stream).  Tensors as for :func:`fa_fwd_splitkv`."""
+    import torch
+
+    B, H, Nq, d = _dims(q)
+    Bk, Hk, Nk, dk = _dims(k)
+    if (Bk, Hk, dk) != (B, H, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q's B, H, d")
+    if tuple(o.shape) != (B, H, Nq, d) or tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("o must be [B, H, Nq, d] and lse [B, H, Nq]")
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor on q's device")
+    with torch.cuda.device(q.device):
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        rc = load_library().fa_fwd_splitkv_static(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
+            d, int(bool(causal)), float(scale), int(num_splits), handle or None)
+        _check(rc, "fa_fwd_splitkv_static")
 
 
 def fa_get_device_status() -> int:

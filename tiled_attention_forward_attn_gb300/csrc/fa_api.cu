@@ -334,6 +334,104 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   return d == 64 ? launch_split<64>(mk, mv, prm, s) : launch_split<128>(mk, mv, prm, s);
 }
 
+// ----------------------------------------------------------------------------
+// fa_fwd_splitkv_static: the split-KV path with its scratch in a buffer that
+// is part of the library, for callers that cannot allocate device memory
+// (code running inside a memory pool or arena that owns all device memory,
+// real-time or capture-time callers for which a cudaMalloc's implicit
+// synchronisation or failure is not acceptable, plug-ins whose host gives
+// them no allocator).
+//
+// The buffer is a file-scope device array: every GPU that loads this library
+// holds kStaticScratchBytes of it until the process exits.  Its name is only
+// a host-side handle; the device address comes from cudaGetSymbolAddress,
+// taken once per device (with that device current) on the first call there.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_splitkv_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on `dev` (the current device).
+int static_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) != cudaSuccess || ptr == nullptr)
+      return FA_ERR_LAUNCH;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t fa_fwd_splitkv_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" int fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int B, int H, int Nq, int Nk, int d, int causal,
+                                     float scale, int num_splits, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  const int shape = split_shape_ok(B, H, Nq, Nk, d, causal, num_splits);
+  if (shape != FA_OK) return shape;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) &
+      15u)
+    return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const size_t q_bytes = static_cast<size_t>(BH) * Nq * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(BH) * Nk * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * Nq * 4;
+  for (const void* in : {q, k, v}) {
+    const size_t n = (in == q) ? q_bytes : kv_bytes;
+    if (overlaps(o, q_bytes, in, n) || overlaps(lse, lse_bytes, in, n)) return FA_ERR_ALIAS;
+  }
+  if (overlaps(o, q_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
+  if (prep != FA_OK) return prep;
+  int splits = 0, kps = 0;
+  split_geometry(BH, Nk, num_splits, sms, &splits, &kps);
+  if (split_ws_bytes(splits, BH, Nq, d) > kStaticScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  const int got = static_scratch(dev, &scratch);
+  if (got != FA_OK) return got;
+
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return FA_ERR_LAUNCH;
+  CUtensorMap mk, mv;
+  if (!encode_map(&mk, k, static_cast<int>(BH), Nk, d, fa::kSplitTileKeys) ||
+      !encode_map(&mv, v, static_cast<int>(BH), Nk, d, fa::kSplitTileKeys))
+    return FA_ERR_LAUNCH;
+
+  // Nothing in the scratch has to start at zero: pass 1 writes every partial
+  // output and log-sum-exp that pass 2 reads.
+  fa::SplitParams prm;
+  prm.q = static_cast<const uint16_t*>(q);
+  prm.o = static_cast<uint16_t*>(o);
+  prm.lse = lse;
+  const size_t rows = static_cast<size_t>(splits) * BH * Nq;
+  prm.ws_o = static_cast<float*>(scratch);
+  prm.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
+                                        round_up(rows * d * 4, kWsAlign));
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.num_bh = static_cast<int>(BH);
+  prm.splits = splits;
+  prm.keys_per_split = kps;
+  prm.causal = causal;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_split<64>(mk, mv, prm, s) : launch_split<128>(mk, mv, prm, s);
+}
+
 extern "C" const char* fa_strerror(int code) {
   switch (code) {
     case FA_OK: return "success";
@@ -347,6 +445,9 @@ extern "C" const char* fa_strerror(int code) {
     case FA_ERR_LAUNCH: return "CUDA error while preparing or launching the kernel";
     case FA_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_fwd_splitkv_workspace_bytes()";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "request needs more scratch than fa_fwd_splitkv_static's built-in buffer holds "
+             "(see fa_fwd_splitkv_static_scratch_bytes(); use fa_fwd_splitkv with a workspace)";
     default: return "unknown error code";
   }
 }
