@@ -46,7 +46,11 @@ L2_FLUSH_BYTES = 256 << 20
 # Per-launch DRAM traffic of the attention kernel on this workload, from an
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum); None until the
 # kernel it was taken on is the one benchmarked.
-NCU_TRAFFIC_BYTES_DECODE = {}  # workload name -> bytes per launch pair, from ncu
+# DRAM bytes (read + write) of one split-pass launch, from one ncu capture
+# per workload (profiles/); the combine pass reads the partials from L2.
+NCU_TRAFFIC_BYTES_DECODE = {
+    "decode_b4h16q16k16384d128_causal": 540_661_760,
+}
 NCU_TRAFFIC_BYTES = 131_094_272  # 122.52 MB read + 8.57 MB written (profiles/fa_fwd_kernel_b2h16n4096d128_causal.md)
 
 
