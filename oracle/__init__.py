@@ -68,6 +68,11 @@ def _load():
                                                   ctypes.c_int, ctypes.c_double, _i64p,
                                                   ctypes.c_int64, _f64p, _f64p, _f64p,
                                                   ctypes.c_int]
+            lib.oracle_attention_rect_fmt.restype = ctypes.c_int
+            lib.oracle_attention_rect_fmt.argtypes = lib.oracle_attention_rect.argtypes + [
+                ctypes.c_int]
+            lib.oracle_f16_to_double.restype = ctypes.c_double
+            lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_attention.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_double,
@@ -100,6 +105,17 @@ def bf16_to_f64(bits) -> np.ndarray:
     flat = _u16(bits).ravel()
     return np.array([lib.oracle_bf16_to_double(int(b)) for b in flat],
                     dtype=np.float64).reshape(np.shape(bits))
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    """Exact widening of IEEE binary16 bit patterns to fp64 (elementwise)."""
+    lib = _load()
+    flat = _u16(bits).ravel()
+    return np.array([lib.oracle_f16_to_double(int(b)) for b in flat],
+                    dtype=np.float64).reshape(np.shape(bits))
+
+
+_FORMATS = {"bf16": 0, "f16": 1}
 
 
 def safe_softmax(x):
@@ -137,10 +153,11 @@ def scores(q, k, scale: float = 1.0, causal: bool = False, row_offset: int = 0):
 
 
 def attention(q, k, v, causal: bool, scale: float, rows=None,
-              return_probs: bool = False, threads: int = 0):
-    """Exact attention forward on bf16 inputs, in fp64.
+              return_probs: bool = False, threads: int = 0, dtype: str = "bf16"):
+    """Exact attention forward on bf16 (or fp16) inputs, in fp64.
 
-    q: uint16 bf16 bit patterns shaped ``[..., Nq, d]``; k, v: ``[..., Nk, d]``
+    q: uint16 bit patterns (``dtype`` "bf16" or "f16") shaped ``[..., Nq, d]``;
+    k, v: ``[..., Nk, d]``
     (leading dims equal and flattened into independent slices).  Causal
     masking is aligned to the end of the keys: query i sees keys
     ``0 .. Nk - Nq + i`` (``0 .. i`` when Nq == Nk).  ``rows``: optional 1-D
@@ -165,10 +182,13 @@ def attention(q, k, v, causal: bool, scale: float, rows=None,
     o = np.empty((BH, n_rows, d))
     lse = np.empty((BH, n_rows))
     p = np.empty((BH, n_rows, Nk)) if return_probs else None
-    rc = lib.oracle_attention_rect(
+    if dtype not in _FORMATS:
+        raise ValueError(f"dtype must be one of {sorted(_FORMATS)}")
+    rc = lib.oracle_attention_rect_fmt(
         _ptr(q, _u16p), _ptr(k, _u16p), _ptr(v, _u16p), BH, Nq, Nk, d, int(bool(causal)),
         float(scale), None if rows_arr is None else _ptr(rows_arr, _i64p), n_rows,
-        _ptr(o, _f64p), _ptr(lse, _f64p), None if p is None else _ptr(p, _f64p), int(threads))
+        _ptr(o, _f64p), _ptr(lse, _f64p), None if p is None else _ptr(p, _f64p), int(threads),
+        _FORMATS[dtype])
     if rc != 0:
         raise ValueError(f"oracle_attention_rect failed with code {rc}")
     o = o.reshape(lead + (n_rows, d))

@@ -17,8 +17,10 @@
  *   - causal masking: query i of Nq sits at position Nk - Nq + i of the Nk
  *     keys and sees keys 0..Nk-Nq+i (square attention: keys 0..i).
  *
- * Inputs are bf16 bit patterns (uint16); each is widened to fp64 exactly.
- * Every floating-point step below runs in fp64.
+ * Inputs are 16-bit bit patterns (uint16) of bf16 or, for the fp16 variant
+ * ("pwwt.cn FlashAttention/Triton walkthrough" §3.4 runs in fp16; §5 lists
+ * fp16 among the extensions), IEEE binary16; each is widened to fp64
+ * exactly.  Every floating-point step below runs in fp64.
  */
 #include <math.h>
 #include <stdint.h>
@@ -35,6 +37,56 @@ double oracle_bf16_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * Exact widening of an IEEE 754 binary16 bit pattern: sign bit, 5-bit
+ * exponent with bias 15, 10-bit fraction; exponent 0 holds zeros and
+ * subnormals (fraction * 2^-24), exponent 31 infinities and NaNs.
+ */
+double oracle_f16_to_double(uint16_t bits)
+{
+    int sign = bits >> 15;
+    int e = (bits >> 10) & 31;
+    int frac = bits & 1023;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)frac, -24);
+    else if (e == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + frac), e - 25);
+    return sign ? -mag : mag;
+}
+
+/* Element formats of the 16-bit inputs. */
+enum { ORACLE_BF16 = 0, ORACLE_F16 = 1 };
+
+static double widen(uint16_t bits, int fmt)
+{
+    return fmt == ORACLE_F16 ? oracle_f16_to_double(bits) : oracle_bf16_to_double(bits);
+}
+
+/*
+ * One row of scores (page 1 §1.1; page 2 causal passage), inputs of format
+ * fmt:
+ *   s_j = scale * sum_t q_t * k_{j,t}     for visible j,
+ *   s_j = -inf                           for j > i when causal.
+ */
+static void score_row_fmt(const uint16_t *q_row, const uint16_t *k, int64_t i,
+                          int64_t n_keys, int64_t d, double scale, int causal,
+                          int fmt, double *s)
+{
+    for (int64_t j = 0; j < n_keys; ++j) {
+        if (causal && j > i) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t)
+            dot += widen(q_row[t], fmt) * widen(k[j * d + t], fmt);
+        s[j] = scale * dot;
+    }
 }
 
 /*
@@ -104,8 +156,8 @@ void oracle_scores(const uint16_t *q, const uint16_t *k, int64_t nq,
  * with Nq queries against Nk keys.  Causal masking is aligned to the end of
  * the key sequence: query i sits at position Nk - Nq + i and sees keys
  * j <= Nk - Nq + i (for Nq == Nk this is the square rule j <= i).
- *   q       : [BH][Nq][d] bf16 bit patterns
- *   k, v    : [BH][Nk][d] bf16 bit patterns
+ *   q       : [BH][Nq][d] 16-bit patterns of format fmt (ORACLE_BF16 / ORACLE_F16)
+ *   k, v    : [BH][Nk][d] 16-bit patterns of format fmt
  *   rows    : n_rows query indices (each in [0, Nq)), applied to every slice;
  *             NULL means all rows (n_rows must then equal Nq)
  *   o_out   : [BH][n_rows][d] fp64,   O_i = sum_j P_ij v_j
@@ -113,12 +165,14 @@ void oracle_scores(const uint16_t *q, const uint16_t *k, int64_t nq,
  *   p_out   : optional [BH][n_rows][Nk] fp64 probabilities (may be NULL)
  * Returns 0, or -1 on bad arguments / -2 on allocation failure.
  */
-int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
-                          double scale, const int64_t *rows, int64_t n_rows,
-                          double *o_out, double *lse_out, double *p_out, int n_threads)
+int oracle_attention_rect_fmt(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                              double scale, const int64_t *rows, int64_t n_rows,
+                              double *o_out, double *lse_out, double *p_out, int n_threads,
+                              int fmt)
 {
     if (!q || !k || !v || !o_out || !lse_out) return -1;
+    if (fmt != ORACLE_BF16 && fmt != ORACLE_F16) return -1;
     if (BH <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || n_rows <= 0) return -1;
     if (causal && Nq > Nk) return -1; /* some query would see no key */
     if (!rows && n_rows != Nq) return -1;
@@ -153,7 +207,7 @@ int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *
             const uint16_t *vh = v + bh * Nk * d;
 
             /* position of query i among the keys (end-aligned) */
-            oracle_score_row(qh, kh, Nk - Nq + i, Nk, d, scale, causal, s);
+            score_row_fmt(qh, kh, Nk - Nq + i, Nk, d, scale, causal, fmt, s);
             double m, l;
             oracle_safe_softmax(s, Nk, NULL, p, &m, &l);
 
@@ -162,7 +216,7 @@ int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *
             for (int64_t j = 0; j < Nk; ++j) {
                 if (p[j] == 0.0) continue; /* masked keys add 0 * v_j */
                 for (int64_t t = 0; t < d; ++t)
-                    o[t] += p[j] * oracle_bf16_to_double(vh[j * d + t]);
+                    o[t] += p[j] * widen(vh[j * d + t], fmt);
             }
             lse_out[bh * n_rows + r] = m + log(l);
             if (p_out)
@@ -173,6 +227,16 @@ int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *
         free(p);
     }
     return failed ? -2 : 0;
+}
+
+/* oracle_attention_rect_fmt on bf16 inputs. */
+int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                          double scale, const int64_t *rows, int64_t n_rows,
+                          double *o_out, double *lse_out, double *p_out, int n_threads)
+{
+    return oracle_attention_rect_fmt(q, k, v, BH, Nq, Nk, d, causal, scale, rows, n_rows,
+                                     o_out, lse_out, p_out, n_threads, ORACLE_BF16);
 }
 
 /*

@@ -8,7 +8,8 @@ CUDA side receive the same bf16 bit patterns from here.
 Recipe (the same on every machine): numpy ``PCG64(seed)``; Q, K, V drawn in
 that order as fp32 ``standard_normal`` of shape ``[B, H, N, d]``; Q and K
 multiplied by ``qk_std`` (3.0 for the large-dynamic-range case); each value
-rounded to bf16 with round-to-nearest-even on its fp32 bits.
+rounded to bf16 with round-to-nearest-even on its fp32 bits (or, for the
+fp16 variants, to IEEE binary16 by numpy's nearest-even conversion).
 """
 from __future__ import annotations
 
@@ -32,6 +33,7 @@ class Workload:
     # "all": the oracle checks every row; "sampled": 512 seeded rows per head
     # plus the boundary rows of the tiling.
     rows: str = "all"
+    dtype: str = "bf16"  # element type of Q, K, V, O: "bf16" or "f16"
 
     @property
     def flops(self) -> float:
@@ -61,6 +63,16 @@ WORKLOADS = (
 )
 
 HEADLINE = WORKLOADS[2]
+
+# The headline shape in fp16, and at head dimension 96 (a multiple of 16
+# below the 128-column layout): the element-type and head-dimension
+# variants of the forward.
+VARIANT_WORKLOADS = (
+    Workload("b2h16n4096d128_causal_fp16", 2, 16, 4096, 128, True, 1.0 / math.sqrt(128), seed=7,
+             rows="sampled", dtype="f16"),
+    Workload("b2h16n4096d96_causal", 2, 16, 4096, 96, True, 1.0 / math.sqrt(96), seed=8,
+             rows="sampled"),
+)
 
 # Sequence lengths that are not multiples of any tile size, checked at both
 # head dimensions, causal and not (B=1, H=2).
@@ -105,7 +117,7 @@ DECODE_WORKLOADS = (
 
 
 def by_name(name: str):
-    for w in WORKLOADS + DECODE_WORKLOADS:
+    for w in WORKLOADS + VARIANT_WORKLOADS + DECODE_WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)
@@ -137,20 +149,29 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to IEEE binary16 (numpy, nearest even); returns
+    uint16 bit patterns."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
 def generate(w: Workload):
-    """Return ``(q, k, v)`` as uint16 bf16 bit patterns ``[B, H, N, d]``."""
-    return generate_shape(w.B, w.H, w.N, w.d, seed=w.seed, qk_std=w.qk_std)
+    """Return ``(q, k, v)`` as uint16 bit patterns ``[B, H, N, d]`` of the
+    workload's element type."""
+    return generate_shape(w.B, w.H, w.N, w.d, seed=w.seed, qk_std=w.qk_std, dtype=w.dtype)
 
 
-def generate_shape(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0):
+def generate_shape(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
+                   dtype: str = "bf16"):
     rng = np.random.Generator(np.random.PCG64(seed))
     shape = (B, H, N, d)
+    to_bits = f32_to_f16_bits if dtype == "f16" else f32_to_bf16_bits
     out = []
     for mult in (qk_std, qk_std, 1.0):
         x = rng.standard_normal(size=shape, dtype=np.float32)
         if mult != 1.0:
             x *= np.float32(mult)
-        out.append(f32_to_bf16_bits(x))
+        out.append(to_bits(x))
     return tuple(out)
 
 
@@ -174,6 +195,15 @@ def as_torch_bf16(bits: np.ndarray):
     import torch
 
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def as_torch(bits: np.ndarray, dtype: str = "bf16"):
+    """View uint16 bit patterns as a CPU tensor of ``dtype`` ("bf16" or
+    "f16"); the bits are reinterpreted, not converted."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
 def torch_bf16_to_bits(t) -> np.ndarray:
