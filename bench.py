@@ -43,15 +43,15 @@ DECODE_METRIC = "split-KV decode attention GB/s of algorithmic HBM bytes & % of 
 DECODE_UNIT = "GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-# Per-launch DRAM traffic of the attention kernel on this workload, from an
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum); None until the
-# kernel it was taken on is the one benchmarked.
 # DRAM bytes (read + write) of one split-pass launch, from one ncu capture
 # per workload (profiles/); the combine pass reads the partials from L2.
 NCU_TRAFFIC_BYTES_DECODE = {
     "decode_b4h16q16k16384d128_causal": 540_661_760,
 }
-NCU_TRAFFIC_BYTES = 131_094_272  # 122.52 MB read + 8.57 MB written (profiles/fa_fwd_kernel_b2h16n4096d128_causal.md)
+# Per-launch DRAM traffic of the forward kernel per workload, from an ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
+# out until a capture of the kernel as benchmarked exists.
+NCU_TRAFFIC_BYTES = {}
 
 
 def load_peaks():
@@ -194,7 +194,8 @@ def cpu_oracle_sample(w, qkv, rows_per_head: int, seed: int, threads: int = 0):
     visible = (rows + 1) if w.causal else np.full(rows.size, w.N)
     flops = float(4.0 * w.d * visible.sum() * w.B * w.H)
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads)
+    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads,
+                     dtype=getattr(w, "dtype", "bf16"))
     dt = time.perf_counter() - t0
     return dt, flops, rows.size, oracle.max_threads() if threads <= 0 else threads
 
@@ -281,7 +282,8 @@ def run_ours(args, w):
 
     decode = isinstance(w, workloads.DecodeWorkload)
     q, k, v = workloads.generate_decode(w) if decode else workloads.generate(w)
-    qd, kd, vd = (workloads.as_torch_bf16(a).to(dev) for a in (q, k, v))
+    elem = getattr(w, "dtype", "bf16")
+    qd, kd, vd = (workloads.as_torch(a, elem).to(dev) for a in (q, k, v))
     o = torch.empty_like(qd)
     lse = torch.empty(tuple(qd.shape[:3]), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -328,7 +330,7 @@ def run_ours(args, w):
 
     # End to end through the same C ABI: pinned host inputs -> device,
     # attention, device -> pinned host outputs, every step.
-    hq, hk, hv = (workloads.as_torch_bf16(a).pin_memory() for a in (q, k, v))
+    hq, hk, hv = (workloads.as_torch(a, elem).pin_memory() for a in (q, k, v))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
@@ -417,7 +419,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": kernel_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": elem, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "causal": w.causal, "scale": w.scale,
                        "l2": "flushed between launches (256 MiB write, untimed)",
@@ -425,8 +427,10 @@ def run_ours(args, w):
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peaks_src} bf16_tflops (burst)",
-                         "traffic": NCU_TRAFFIC_BYTES},
+                         "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
+                             "; fp16 x 1: its nominal dense rate equals bf16's"
+                             if elem == "f16" else ""),
+                         "traffic": NCU_TRAFFIC_BYTES.get(w.name)},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -449,7 +453,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=workloads.HEADLINE.name,
-                    choices=[x.name for x in workloads.WORKLOADS + workloads.DECODE_WORKLOADS])
+                    choices=[x.name for x in workloads.WORKLOADS + workloads.VARIANT_WORKLOADS
+                             + workloads.DECODE_WORKLOADS])
     ap.add_argument("--cpu-rows", type=int, default=512,
                     help="query rows per head timed for the CPU baseline")
     ap.add_argument("--ref-rows", type=int, default=64,

@@ -30,6 +30,7 @@
 #define FA_H_
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -47,8 +48,14 @@ enum fa_status {
   FA_ERR_LAUNCH = 8,    /* CUDA runtime / driver error while preparing or launching */
   FA_ERR_TIMEOUT = 9,   /* a kernel wait exceeded its limit (see fa_get_device_status) */
   FA_ERR_WORKSPACE = 10, /* split-KV workspace NULL or too small */
-  FA_ERR_SCRATCH_LIMIT = 11 /* fa_fwd_splitkv_static: request exceeds its built-in scratch */
+  FA_ERR_SCRATCH_LIMIT = 11, /* fa_fwd_splitkv_static: request exceeds its built-in scratch */
+  FA_ERR_DTYPE = 12,    /* element type not FA_DTYPE_BF16 / FA_DTYPE_FP16 */
+  FA_ERR_STRIDE = 13    /* invalid strides, or overlapping output elements */
 };
+
+/* Element types of Q, K, V and O (fa_fwd_strided). */
+#define FA_DTYPE_BF16 0
+#define FA_DTYPE_FP16 1
 
 /*
  * fa_fwd — attention forward for all (batch, head) slices.
@@ -58,7 +65,7 @@ enum fa_status {
  *   lse     : fp32 [B][H][N], contiguous (device), written; natural-log units
  *             of the scaled, masked scores: LSE_i = ln sum_j exp(S_ij)
  *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1
- *   d       : head dimension, 64 or 128
+ *   d       : head dimension, a multiple of 16 from 16 to 128
  *   causal  : 0 = full attention, 1 = query i sees keys 0..i (square,
  *             top-left aligned)
  *   scale   : any finite float multiplying Q K^T (typically 1/sqrt(d))
@@ -71,6 +78,29 @@ enum fa_status {
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
            int d, int causal, float scale, void *stream);
+
+/*
+ * fa_fwd_strided — fa_fwd with a choice of element type and arbitrary
+ * strides ("pwwt.cn FlashAttention/Triton walkthrough" §3.4 passes every
+ * tensor with its batch, head and row strides; §5 lists fp16 and other head
+ * dimensions among the extensions).
+ *
+ *   q, k, v, o : [B][H][N][d] tensors of `dtype` elements (device, base
+ *                16-byte aligned); element (b, h, n, c) of tensor X lives at
+ *                X + b*X_strides[0] + h*X_strides[1] + n*X_strides[2] + c
+ *   *_strides  : 3 int64 element strides (batch, head, row), each a
+ *                non-negative multiple of 8 below 2^38; NULL = contiguous
+ *                [B][H][N][d].  Columns are always contiguous.  Distinct
+ *                elements of o must not overlap (FA_ERR_STRIDE).
+ *   lse        : fp32 [B][H][N], contiguous (device), written
+ *   dtype      : FA_DTYPE_BF16 or FA_DTYPE_FP16 (the P.V operand P takes the
+ *                same type; accumulation and statistics are fp32)
+ *   other arguments and the result as for fa_fwd.
+ */
+int fa_fwd_strided(const void *q, const int64_t *q_strides, const void *k,
+                   const int64_t *k_strides, const void *v, const int64_t *v_strides, void *o,
+                   const int64_t *o_strides, float *lse, int dtype, int B, int H, int N, int d,
+                   int causal, float scale, void *stream);
 
 /*
  * fa_fwd_splitkv — attention of a short block of queries against a long key

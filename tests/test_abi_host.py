@@ -74,9 +74,55 @@ def test_bad_shapes_rejected(lib, kw):
     assert _call(lib, **kw) == FA_ERR_SHAPE
 
 
-@pytest.mark.parametrize("d", [0, 16, 32, 96, 127, 256])
+@pytest.mark.parametrize("d", [0, 8, 24, 127, 144, 256])
 def test_unsupported_head_dim_rejected(lib, d):
     assert _call(lib, d=d) == FA_ERR_HEAD_DIM
+
+
+@pytest.mark.parametrize("d", [16, 32, 48, 80, 96, 112])
+def test_multiple_of_16_head_dims_accepted(lib, d):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present; covered by the GPU tests")
+    # Validation passes; only the missing device stops the call.
+    assert _call(lib, d=d) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
+FA_ERR_DTYPE, FA_ERR_STRIDE = 12, 13
+
+
+def _strided(lib, qs=None, ks=None, vs=None, os_=None, dtype=0, B=2, H=3, N=100, d=64, o=None,
+             lse=None):
+    def arr(st):
+        return None if st is None else (ctypes.c_int64 * 3)(*st)
+
+    big = 1 << 24  # buffers far apart: no aliasing unless intended
+    o = 4 * big if o is None else o
+    lse = 5 * big if lse is None else lse
+    return lib.fa_fwd_strided(big, arr(qs), 2 * big, arr(ks), 3 * big, arr(vs), o, arr(os_), lse,
+                              dtype, B, H, N, d, 0, 0.1, None)
+
+
+def test_strided_validation(lib):
+    import torch
+
+    no_dev = not torch.cuda.is_available()
+    assert _strided(lib, dtype=2) == FA_ERR_DTYPE
+    assert _strided(lib, qs=(-64, 64, 64)) == FA_ERR_STRIDE  # negative
+    assert _strided(lib, ks=(19200, 6400, 68)) == FA_ERR_STRIDE  # not a multiple of 8
+    assert _strided(lib, vs=(1 << 38, 64, 64)) == FA_ERR_STRIDE  # too large
+    # o rows overlapping (row stride below d), o heads overlapping
+    assert _strided(lib, os_=(19200, 6400, 32)) == FA_ERR_STRIDE
+    assert _strided(lib, os_=(19200, 64, 64)) == FA_ERR_STRIDE
+    # [B, N, H, d] memory viewed as [B, H, N, d] is disjoint; so are padded rows
+    # and inputs shared across heads (stride 0).
+    if no_dev:
+        for kw in (dict(os_=(19200, 64, 192)), dict(os_=(20000, 6400, 64)),
+                   dict(ks=(6400, 0, 64), vs=(6400, 0, 64)), dict(dtype=1)):
+            assert _strided(lib, **kw) in (FA_ERR_LAUNCH, FA_ERR_DEVICE), kw
+    # the output's strided span overlapping an input is aliasing
+    assert _strided(lib, o=3 * (1 << 24) + 4096, os_=(19200, 64, 192)) == FA_ERR_ALIAS
 
 
 @pytest.mark.parametrize("kw", [dict(q=A16 + 2), dict(k=2 * A16 + 8), dict(v=3 * A16 + 1),

@@ -17,7 +17,7 @@ import threading
 from . import _build
 
 __all__ = [
-    "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version",
+    "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version", "fa_fwd_strided",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
@@ -56,6 +56,10 @@ def load_library(path: str | None = None):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.fa_fwd.restype = i
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.fa_fwd_strided.restype = i
+        lib.fa_fwd_strided.argtypes = [vp, i64p, vp, i64p, vp, i64p, vp, i64p, vp, i, i, i, i, i,
+                                       i, f, vp]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_strerror.argtypes = [i]
         lib.fa_get_device_status.restype = i
@@ -109,11 +113,33 @@ def _dims(t):
     return tuple(int(x) for x in t.shape)
 
 
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP16 = 1
+
+
+def fa_fwd_strided(q_ptr: int, q_strides, k_ptr: int, k_strides, v_ptr: int, v_strides,
+                   o_ptr: int, o_strides, lse_ptr: int, dtype: int, B: int, H: int, N: int,
+                   d: int, causal: bool, scale: float, stream: int = 0) -> int:
+    """Direct call of the strided entry point; strides are 3-tuples of
+    element strides (batch, head, row) or None; returns the C return code."""
+    def arr(st):
+        if st is None:
+            return None
+        return (ctypes.c_int64 * 3)(*[int(x) for x in st])
+
+    return int(load_library().fa_fwd_strided(
+        q_ptr, arr(q_strides), k_ptr, arr(k_strides), v_ptr, arr(v_strides), o_ptr,
+        arr(o_strides), lse_ptr, int(dtype), int(B), int(H), int(N), int(d), int(bool(causal)),
+        float(scale), stream or None))
+
+
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     """Attention forward into preallocated CUDA tensors.
 
-    q, k, v, o: ``torch.bfloat16`` ``[B, H, N, d]`` contiguous on one CUDA
-    device; lse: ``torch.float32`` ``[B, H, N]``.  Enqueued on ``stream``
+    q, k, v, o: ``[B, H, N, d]`` tensors of one dtype, ``torch.bfloat16`` or
+    ``torch.float16``, on one CUDA device, any strides with the last
+    dimension contiguous (strides multiples of 8 elements); lse:
+    ``torch.float32`` ``[B, H, N]`` contiguous.  Enqueued on ``stream``
     (default: the current torch stream of q's device); asynchronous.
     """
     import torch
@@ -124,36 +150,47 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(B, H, N, d)}")
     if tuple(lse.shape) != (B, H, N):
         raise ValueError(f"lse has shape {tuple(lse.shape)}, expected {(B, H, N)}")
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
-                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
-                        ("lse", lse, torch.float32)):
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"q must be bfloat16 or float16, got {q.dtype}")
+    for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype),
+                        ("o", o, q.dtype), ("lse", lse, torch.float32)):
         if t.dtype != dt:
             raise TypeError(f"{name} must be {dt}, got {t.dtype}")
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
         if t.device != q.device:
             raise ValueError("all tensors must be on one device")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.stride(3) != 1 and d > 1:
+            raise ValueError(f"{name} must have a contiguous last dimension")
+    if not lse.is_contiguous():
+        raise ValueError("lse must be contiguous")
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dtype = FA_DTYPE_FP16 if q.dtype == torch.float16 else FA_DTYPE_BF16
+
+    def st(t):  # a dimension of extent 1 is never stepped: its stride is irrelevant
+        return tuple(0 if t.shape[i] == 1 else t.stride(i) for i in range(3))
+
     with torch.cuda.device(q.device):
-        _check(fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          B, H, N, d, causal, scale, handle), "fa_fwd")
+        _check(fa_fwd_strided(q.data_ptr(), st(q), k.data_ptr(), st(k), v.data_ptr(), st(v),
+                              o.data_ptr(), st(o), lse.data_ptr(), dtype, B, H, N, d, causal,
+                              scale, handle), "fa_fwd")
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
     """Allocate ``O`` (bf16) and ``LSE`` (fp32) and run :func:`fa_fwd`.
 
-    ``scale`` defaults to ``1/sqrt(d)``.  Returns ``(O, LSE)``.
+    ``scale`` defaults to ``1/sqrt(d)``.  O has q's dtype and is contiguous.
+    Returns ``(O, LSE)``.
     """
     import torch
 
     B, H, N, d = _dims(q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    o = torch.empty_like(q)
+    o = torch.empty((B, H, N, d), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse

@@ -44,15 +44,27 @@ void load_encode() {
 // with exactly the per-thread register count its setmaxnreg split assumes
 // (a different count could leave the softmax warpgroups waiting for
 // registers that the pool does not hold).
-template <int D, bool kNeg>
+template <int D, bool kNeg, bool kF16, bool kPartialD>
 cudaError_t configure_kernel() {
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, kNeg>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_fwd_kernel<D, kNeg, kF16, kPartialD>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != static_cast<int>(fa::kLaunchRegs)) return cudaErrorInvalidKernelImage;
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, kNeg>,
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, kNeg, kF16, kPartialD>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::Cfg<D>::kSmemAlloc));
+}
+
+template <int D, bool kF16, bool kPartialD>
+bool configure_both_signs() {
+  return configure_kernel<D, false, kF16, kPartialD>() == cudaSuccess &&
+         configure_kernel<D, true, kF16, kPartialD>() == cudaSuccess;
+}
+
+template <int D>
+bool configure_dim() {
+  return configure_both_signs<D, false, false>() && configure_both_signs<D, true, false>() &&
+         configure_both_signs<D, false, true>() && configure_both_signs<D, true, true>();
 }
 
 template <int D>
@@ -85,8 +97,7 @@ int prepare_device(int* dev_out, int* sms_out) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
-  if (configure_kernel<64, false>() != cudaSuccess || configure_kernel<64, true>() != cudaSuccess ||
-      configure_kernel<128, false>() != cudaSuccess || configure_kernel<128, true>() != cudaSuccess ||
+  if (!configure_dim<64>() || !configure_dim<128>() ||
       configure_split_kernel<64>() != cudaSuccess || configure_split_kernel<128>() != cudaSuccess)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
@@ -95,8 +106,8 @@ int prepare_device(int* dev_out, int* sms_out) {
   return FA_OK;
 }
 
-// [BH][N][d] bf16 viewed as a 3-D tensor (d innermost), boxes of
-// 64 columns x `box_rows` rows x 1 slice with the 128-byte swizzle.
+// Contiguous [BH][N][d] bf16 viewed as a 3-D tensor (d innermost), boxes of
+// 64 columns x `box_rows` rows x 1 slice with the 128-byte swizzle (split-KV).
 bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
@@ -118,27 +129,97 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 // Persistent launch: one CTA per multiprocessor (at most one per work unit);
 // each CTA walks its share of the units inside the kernel.
-template <int D, bool kNeg>
+template <int D, bool kNeg, bool kF16, bool kPartialD>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
            const fa::FwdParams& prm, int sms, cudaStream_t stream) {
   const unsigned ctas = static_cast<unsigned>(prm.total_units < sms ? prm.total_units : sms);
-  fa::fa_fwd_kernel<D, kNeg><<<ctas, fa::kNumThreads, fa::Cfg<D>::kSmemAlloc, stream>>>(
-      mq, mk, mv, prm);
+  fa::fa_fwd_kernel<D, kNeg, kF16, kPartialD>
+      <<<ctas, fa::kNumThreads, fa::Cfg<D>::kSmemAlloc, stream>>>(mq, mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-}  // namespace
+template <int D, bool kF16, bool kPartialD>
+int launch_sign(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                const fa::FwdParams& prm, int sms, cudaStream_t stream) {
+  return prm.scale_log2 < 0.0f ? launch<D, true, kF16, kPartialD>(mq, mk, mv, prm, sms, stream)
+                               : launch<D, false, kF16, kPartialD>(mq, mk, mv, prm, sms, stream);
+}
 
-extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                      int N, int d, int causal, float scale, void* stream) {
+// [B][H][N][d] view with element strides (sb, sh, sn) and unit column stride,
+// as a 4-D tensor map {d, N, H, B}: boxes of 64 columns x 128 rows x 1 x 1
+// with the 128-byte swizzle; columns past d and rows past N read as zero.
+bool encode_map4(CUtensorMap* map, const void* ptr, CUtensorMapDataType type, int B, int H, int N,
+                 int d, const int64_t* st) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  // A dimension of extent 1 is never stepped; give it a harmless stride.
+  auto stride = [&](int i, int extent) -> cuuint64_t {
+    const int64_t bytes = st[i] * 2;
+    return static_cast<cuuint64_t>(extent == 1 && bytes == 0 ? 16 : bytes);
+  };
+  const cuuint64_t strides[3] = {stride(2, N), stride(1, H), stride(0, B)};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  const CUresult r =
+      g_encode(map, type, 4, const_cast<void*>(ptr), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Bytes from the first to one past the last element of a strided
+// [B][H][N][d] tensor of 2-byte elements.
+size_t span_bytes(int B, int H, int N, int d, const int64_t* st) {
+  const int64_t last = (B - 1) * st[0] + (H - 1) * st[1] + (N - 1) * st[2] + d;
+  return static_cast<size_t>(last) * 2;
+}
+
+// Whether distinct (b, h, row, col) of a strided [B][H][N][d] tensor with
+// unit column stride map to distinct addresses: with the dimensions of
+// extent > 1 sorted by stride, each stride must step over the whole extent
+// of the ones below it.
+bool strides_disjoint(int B, int H, int N, int d, const int64_t* st) {
+  int64_t s[3] = {st[0], st[1], st[2]};
+  int64_t n[3] = {B, H, N};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (s[j] < s[i]) {
+        const int64_t ts = s[i], tn = n[i];
+        s[i] = s[j];
+        n[i] = n[j];
+        s[j] = ts;
+        n[j] = tn;
+      }
+  int64_t covered = d;  // extent of the dimensions below, in elements
+  for (int i = 0; i < 3; ++i) {
+    if (n[i] == 1) continue;
+    if (s[i] < covered) return false;
+    covered = s[i] * (n[i] - 1) + covered;
+  }
+  return true;
+}
+
+int fwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* ks_in,
+             const void* v, const int64_t* vs_in, void* o, const int64_t* os_in, float* lse,
+             int dtype, int B, int H, int N, int d, int causal, float scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  if (d < 16 || d > 128 || d % 16 != 0) return FA_ERR_HEAD_DIM;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
   const int64_t BH = static_cast<int64_t>(B) * H;
   const int64_t num_units = (static_cast<int64_t>(N) + fa::kUnitM - 1) / fa::kUnitM;
   // Work units (B*H x 256-row query units) are counted in int, and so are
   // the row offsets bh*N + row of the LSE store.
   if (BH > INT_MAX || BH * num_units > INT_MAX || BH * N > INT_MAX) return FA_ERR_SHAPE;
+  const int64_t contig[3] = {static_cast<int64_t>(H) * N * d, static_cast<int64_t>(N) * d, d};
+  const int64_t* qs = qs_in ? qs_in : contig;
+  const int64_t* ks = ks_in ? ks_in : contig;
+  const int64_t* vs = vs_in ? vs_in : contig;
+  const int64_t* os = os_in ? os_in : contig;
+  for (const int64_t* st : {qs, ks, vs, os})
+    for (int i = 0; i < 3; ++i)
+      if (st[i] < 0 || st[i] % 8 != 0 || st[i] >= (int64_t(1) << 38)) return FA_ERR_STRIDE;
+  if (!strides_disjoint(B, H, N, d, os)) return FA_ERR_STRIDE;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) &
       15u)
@@ -146,13 +227,15 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
   if (!std::isfinite(scale)) return FA_ERR_SCALE;
   if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
-  const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
+  const size_t o_span = span_bytes(B, H, N, d, os);
   const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
-  for (const void* in : {q, k, v}) {
-    if (overlaps(o, tensor_bytes, in, tensor_bytes) || overlaps(lse, lse_bytes, in, tensor_bytes))
-      return FA_ERR_ALIAS;
+  const void* ins[3] = {q, k, v};
+  const int64_t* in_st[3] = {qs, ks, vs};
+  for (int i = 0; i < 3; ++i) {
+    const size_t n = span_bytes(B, H, N, d, in_st[i]);
+    if (overlaps(o, o_span, ins[i], n) || overlaps(lse, lse_bytes, ins[i], n)) return FA_ERR_ALIAS;
   }
-  if (overlaps(o, tensor_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+  if (overlaps(o, o_span, lse, lse_bytes)) return FA_ERR_ALIAS;
 
   int dev = 0, sms = 0;
   const int prep = prepare_device(&dev, &sms);
@@ -160,16 +243,26 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   std::call_once(g_encode_once, load_encode);
   if (g_encode == nullptr) return FA_ERR_LAUNCH;
 
+  const CUtensorMapDataType tt =
+      dtype == FA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv;
-  if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
-      !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
-      !encode_map(&mv, v, static_cast<int>(BH), N, d))
+  if (!encode_map4(&mq, q, tt, B, H, N, d, qs) || !encode_map4(&mk, k, tt, B, H, N, d, ks) ||
+      !encode_map4(&mv, v, tt, B, H, N, d, vs))
     return FA_ERR_LAUNCH;
 
+  const bool f16 = dtype == FA_DTYPE_FP16;
   fa::FwdParams prm;
   prm.o = static_cast<uint16_t*>(o);
   prm.lse = lse;
+  prm.o_sb = os[0];
+  prm.o_sh = os[1];
+  prm.o_sn = os[2];
   prm.N = N;
+  prm.H = H;
+  prm.d = d;
+  prm.k_slices = d / 16;
+  prm.idesc_pv = f16 ? fa::idesc_f16_f32(fa::kTileM, static_cast<uint32_t>(d), 0, 1)
+                     : fa::idesc_bf16_f32(fa::kTileM, static_cast<uint32_t>(d), 0, 1);
   prm.num_bh = static_cast<int>(BH);
   prm.num_units = static_cast<int>(num_units);
   prm.total_units = static_cast<int>(BH * num_units);
@@ -183,11 +276,34 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   prm.inject = g_inject.load(std::memory_order_relaxed);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool neg = prm.scale_log2 < 0.0f;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 128)
+    return f16 ? launch_sign<128, true, false>(mq, mk, mv, prm, sms, st)
+               : launch_sign<128, false, false>(mq, mk, mv, prm, sms, st);
   if (d == 64)
-    return neg ? launch<64, true>(mq, mk, mv, prm, sms, s) : launch<64, false>(mq, mk, mv, prm, sms, s);
-  return neg ? launch<128, true>(mq, mk, mv, prm, sms, s) : launch<128, false>(mq, mk, mv, prm, sms, s);
+    return f16 ? launch_sign<64, true, false>(mq, mk, mv, prm, sms, st)
+               : launch_sign<64, false, false>(mq, mk, mv, prm, sms, st);
+  if (d > 64)
+    return f16 ? launch_sign<128, true, true>(mq, mk, mv, prm, sms, st)
+               : launch_sign<128, false, true>(mq, mk, mv, prm, sms, st);
+  return f16 ? launch_sign<64, true, true>(mq, mk, mv, prm, sms, st)
+             : launch_sign<64, false, true>(mq, mk, mv, prm, sms, st);
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int N, int d, int causal, float scale, void* stream) {
+  return fwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, FA_DTYPE_BF16, B, H, N, d,
+                  causal, scale, stream);
+}
+
+extern "C" int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k,
+                              const int64_t* k_strides, const void* v, const int64_t* v_strides,
+                              void* o, const int64_t* o_strides, float* lse, int dtype, int B,
+                              int H, int N, int d, int causal, float scale, void* stream) {
+  return fwd_impl(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, dtype, B, H, N, d,
+                  causal, scale, stream);
 }
 
 // ---------------------------------------------------------------- split-KV
@@ -437,7 +553,8 @@ extern "C" const char* fa_strerror(int code) {
     case FA_OK: return "success";
     case FA_ERR_NULL: return "a required pointer is NULL";
     case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and within index limits; causal 0 or 1)";
-    case FA_ERR_HEAD_DIM: return "unsupported head dimension (d must be 64 or 128)";
+    case FA_ERR_HEAD_DIM:
+      return "unsupported head dimension (fa_fwd: a multiple of 16 in 16..128; split-KV: 64 or 128)";
     case FA_ERR_ALIGN: return "misaligned pointer (q, k, v, o need 16 bytes; lse needs 4)";
     case FA_ERR_SCALE: return "scale is not finite";
     case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
@@ -445,6 +562,10 @@ extern "C" const char* fa_strerror(int code) {
     case FA_ERR_LAUNCH: return "CUDA error while preparing or launching the kernel";
     case FA_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_fwd_splitkv_workspace_bytes()";
+    case FA_ERR_DTYPE: return "unsupported element type (FA_DTYPE_BF16 or FA_DTYPE_FP16)";
+    case FA_ERR_STRIDE:
+      return "invalid strides (non-negative multiples of 8 elements below 2^38; o's elements "
+             "must not overlap)";
     case FA_ERR_SCRATCH_LIMIT:
       return "request needs more scratch than fa_fwd_splitkv_static's built-in buffer holds "
              "(see fa_fwd_splitkv_static_scratch_bytes(); use fa_fwd_splitkv with a workspace)";

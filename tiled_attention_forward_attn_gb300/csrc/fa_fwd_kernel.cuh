@@ -45,6 +45,16 @@
 // and O keep sharing one reference and the result is unchanged; most tiles
 // then need no O rescale at all.
 //
+// Element types and shapes: Q, K, V and O are bf16 or fp16 (kF16; both MMA
+// operands always share the type, P included), the accumulation and the
+// softmax statistics fp32.  The shared-memory layout is sized for a padded
+// head dimension D (64 or 128); a smaller logical d (a multiple of 16,
+// kPartialD) is read through the same boxes, the columns past d zero-filled
+// by TMA, the Q K^T MMAs stop after d/16 slices, the P.V MMAs produce d
+// columns and the epilogue stores d.  Q, K and V are read through 4-D tensor
+// maps {d, N, H, B} with arbitrary 16-byte-multiple strides; O is stored at
+// arbitrary strides too.
+//
 // Every mbarrier wait is bounded: on expiry the kernel records
 // FA_DEVICE_STATUS_TIMEOUT in a device status word, every role leaves its
 // loop, in-flight copies and MMAs are drained (again bounded), TMEM is freed
@@ -83,9 +93,14 @@ constexpr uint32_t kInjectSkipFirstV = 1u;  // test hook: never issue the first 
 __device__ uint32_t g_fa_status;
 
 struct FwdParams {
-  uint16_t* o;       // [BH][N][D] bf16 bit patterns
-  float* lse;        // [BH][N] fp32
+  uint16_t* o;       // bf16 / fp16 bit patterns: (b, h, row, col) at b*o_sb + h*o_sh + row*o_sn + col
+  float* lse;        // [B][H][N] fp32, contiguous
+  int64_t o_sb, o_sh, o_sn;  // O strides in elements (multiples of 8)
   int N;             // sequence length
+  int H;             // heads (bh = b * H + h)
+  int d;             // logical head dimension (<= D, a multiple of 16)
+  int k_slices;      // d / 16: 16-column slices of the Q K^T product
+  uint32_t idesc_pv; // P.V instruction descriptor producing d columns
   int num_bh;        // B * H
   int num_units;     // ceil(N / kUnitM) query units per (batch, head)
   int total_units;   // num_bh * num_units
@@ -118,8 +133,6 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_t at kColS + 128*t, P_t over its first 64 columns
   static constexpr uint32_t kColO = 256;  // O_t at kColO + D*t
-  static constexpr uint32_t kIdescQK = idesc_bf16_f32(kTileM, kBlockN, 0, 0);
-  static constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileM, D, 0, 1);
 };
 
 // Barrier addresses (8 bytes each) in the order of the layout above.
@@ -197,6 +210,7 @@ __device__ __forceinline__ uint32_t parity_of(uint32_t n) { return n & 1u; }
 // ----------------------------------------------------------------------------
 struct Unit {
   int bh;    // batch * heads + head
+  int b, h;  // batch and head of bh
   int q0;    // first query row of tile A
   int n[2];  // key tiles visited by tiles A and B (0 = tile past the end)
 };
@@ -218,6 +232,8 @@ __device__ __forceinline__ Unit unit_at(int idx, const FwdParams& p) {
   Unit u;
   const int qu = p.num_units - 1 - idx / p.num_bh;
   u.bh = idx % p.num_bh;
+  u.b = u.bh / p.H;
+  u.h = u.bh - u.b * p.H;
   u.q0 = qu * kUnitM;
   u.n[0] = key_tiles_for(u.q0, p.N, p.causal);
   u.n[1] = key_tiles_for(u.q0 + kTileM, p.N, p.causal);
@@ -237,9 +253,9 @@ __device__ __forceinline__ int unit_index(int r) {
 // ----------------------------------------------------------------------------
 // Softmax warps: one query tile of one unit (128 threads, one row each)
 // ----------------------------------------------------------------------------
-template <int D, bool kNegScale>
+template <int D, bool kNegScale, bool kF16, bool kPartialD>
 __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, const int r0,
-                                             const int bh, const uint32_t tmem,
+                                             const Unit& u, const uint32_t tmem,
                                              const Barriers& bars, const WaitCtx& wctx,
                                              const FwdParams& p, uint32_t& s_uses,
                                              uint32_t& o_uses) {
@@ -310,7 +326,7 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
       m_ref = m_new;
     }
 
-    // P = 2^(s*c - m_ref) and its row sum; P_t goes, as bf16 pairs, over the
+    // P = 2^(s*c - m_ref) and its row sum; P_t goes, as 16-bit pairs, over the
     // first 64 columns of S_t (whose values are already in registers), in
     // two halves so that half of the scores are dead before the second.
     const float neg_m = -m_ref;
@@ -328,8 +344,8 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         fadd2(sa0, sa1, sa0, sa1, p0, p1);
         fadd2(sb0, sb1, sb0, sb1, p2, p3);
-        pk[i / 2] = pack_bf16x2(p0, p1);
-        pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+        pk[i / 2] = pack_x2<kF16>(p0, p1);
+        pk[i / 2 + 1] = pack_x2<kF16>(p2, p3);
       }
       tmem_st32(s_addr + 32 * h, pk);
     }
@@ -362,14 +378,14 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
   }
 
   // ---------------------------------------------------------------- epilogue
-  // O = O_t / l as bf16, straight from registers to global memory (each
-  // thread writes its own row, 2*D contiguous bytes), then LSE.
+  // O = O_t / l in the element type, straight from registers to global
+  // memory (each thread writes its own row, 2*d contiguous bytes), then LSE.
   if (!warp_wait_bar(bars.o_done(t), parity_of(o_uses), wctx)) return false;
   ++o_uses;
   tc_fence_after_sync();
   const float inv_l = 1.0f / l_run;
   const bool in_range = q_idx < p.N;
-  uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(bh) * p.N + q_idx) * D);
+  uint4* dst = reinterpret_cast<uint4*>(p.o + u.b * p.o_sb + u.h * p.o_sh + q_idx * p.o_sn);
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t o[32];
@@ -384,17 +400,18 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
         float a0, a1;
         fmul2(a0, a1, __uint_as_float(o[8 * g + 2 * e]), __uint_as_float(o[8 * g + 2 * e + 1]),
               inv_l, inv_l);
-        w4[e] = pack_bf16x2(a0, a1);
+        w4[e] = pack_x2<kF16>(a0, a1);
       }
-      if (in_range) dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      if (in_range && (!kPartialD || 32 * cc + 8 * g < p.d))
+        dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
     }
   }
   if (in_range)
-    p.lse[static_cast<size_t>(bh) * p.N + q_idx] = (m_ref + __log2f(l_run)) * 0.6931471805599453f;
+    p.lse[static_cast<size_t>(u.bh) * p.N + q_idx] = (m_ref + __log2f(l_run)) * 0.6931471805599453f;
   return true;
 }
 
-template <int D, bool kNegScale>
+template <int D, bool kNegScale, bool kF16, bool kPartialD>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -468,8 +485,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const Unit u = unit_at(idx, p);
       const int n = t == 0 ? u.n[0] : u.n[1];
       if (n == 0) continue;
-      if (!softmax_tile<D, kNegScale>(t, n, u.q0 + kTileM * t, u.bh, tmem, bars, wctx, p, s_uses,
-                                      o_uses))
+      if (!softmax_tile<D, kNegScale, kF16, kPartialD>(t, n, u.q0 + kTileM * t, u, tmem, bars,
+                                                        wctx, p, s_uses, o_uses))
         break;
     }
   } else if (warp == kLoadWarp) {
@@ -507,8 +524,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               mbar_arrive_expect_tx(bars.q_full(t), C::kQBytes);
 #pragma unroll
               for (int b = 0; b < D / 64; ++b)
-                tma_load_3d_hint(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t),
-                                 64 * b, u.q0 + kTileM * t, u.bh, once);
+                tma_load_4d_hint(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t),
+                                 64 * b, u.q0 + kTileM * t, u.h, u.b, once);
               ++qc[t];
             }
             if (!ok) break;
@@ -516,8 +533,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d_hint(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s),
-                             64 * b, j * kBlockN, u.bh, keep);
+            tma_load_4d_hint(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s),
+                             64 * b, j * kBlockN, u.h, u.b, keep);
           ++kc;
         }
       }
@@ -561,8 +578,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           mbar_arrive_expect_tx(bars.v_full(s), C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d_hint(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s),
-                             64 * b, j * kBlockN, u.bh, keep);
+            tma_load_4d_hint(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s),
+                             64 * b, j * kBlockN, u.h, u.b, keep);
         }
       }
 #pragma unroll
@@ -583,6 +600,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // run ahead.  The same lane must issue the MMAs and the commits: a
     // commit tracks only the MMAs of its own thread.
     const bool leader = elect_one_sync();
+    constexpr uint32_t kIdescQK = kF16 ? idesc_f16_f32(kTileM, kBlockN, 0, 0)
+                                       : idesc_bf16_f32(kTileM, kBlockN, 0, 0);
+    constexpr uint32_t kIdescPVFull = kF16 ? idesc_f16_f32(kTileM, D, 0, 1)
+                                           : idesc_bf16_f32(kTileM, D, 0, 1);
+    const uint32_t idesc_pv = kPartialD ? p.idesc_pv : kIdescPVFull;
     // Descriptor halves: every operand sits at a fixed SMEM address, so the
     // low halves of all descriptors are a base plus compile-time offsets.
     constexpr uint32_t kHi = desc_hi_sw128(1024);
@@ -604,8 +626,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lohi(d_tmem, a_lo + kmaj_off(kk), kHi, b_lo + kmaj_off(kk), kHi, C::kIdescQK,
-                       kk > 0 ? 1u : 0u);
+          if (!kPartialD || kk < p.k_slices)
+            umma_ss_lohi(d_tmem, a_lo + kmaj_off(kk), kHi, b_lo + kmaj_off(kk), kHi, kIdescQK,
+                         kk > 0 ? 1u : 0u);
       }
       __syncwarp();
     };
@@ -617,7 +640,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)  // V slice kk: 16 key rows of 128 bytes
-          umma_ts_lohi(d_tmem, p_tmem + 8u * kk, b_lo + ((kk * 16 * 128) >> 4), kHi, C::kIdescPV,
+          umma_ts_lohi(d_tmem, p_tmem + 8u * kk, b_lo + ((kk * 16 * 128) >> 4), kHi, idesc_pv,
                        kk > 0 ? 1u : acc0);
       }
       __syncwarp();

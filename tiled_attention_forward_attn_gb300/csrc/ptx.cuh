@@ -109,6 +109,17 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// 4-D tiled load (coordinates x innermost .. w outermost) with an L2 cache hint.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t x, int32_t y, int32_t z,
+                                                 int32_t w, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
+
 // L2 policies: keep lines that later loads will reuse / drop lines read once.
 __device__ __forceinline__ uint64_t make_l2_policy_evict_last() {
   uint64_t pol;
@@ -251,6 +262,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same for fp16 A and B (operand format field 0 instead of 1 = bf16).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t a_mn_major,
+                                                     uint32_t b_mn_major) {
+  return (1u << 4) | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05: TMEM <-> registers (32 data-path lanes x 32 bits, 32 columns)
 // Thread t of warp w reads/writes TMEM lane 32*(w%4)+t, columns [col, col+32).
@@ -322,6 +340,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 values to one 16-bit pair of the element type (bf16 or fp16).
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
+  return kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 // Packed pair arithmetic (one instruction for two fp32 lanes).
