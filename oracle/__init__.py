@@ -71,6 +71,11 @@ def _load():
             lib.oracle_attention_rect_fmt.restype = ctypes.c_int
             lib.oracle_attention_rect_fmt.argtypes = lib.oracle_attention_rect.argtypes + [
                 ctypes.c_int]
+            lib.oracle_attention_bwd.restype = ctypes.c_int
+            lib.oracle_attention_bwd.argtypes = [_u16p, _u16p, _u16p, _u16p, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                                 ctypes.c_double, _f64p, _f64p, _f64p,
+                                                 ctypes.c_int, ctypes.c_int]
             lib.oracle_f16_to_double.restype = ctypes.c_double
             lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_attention.restype = ctypes.c_int
@@ -196,3 +201,31 @@ def attention(q, k, v, causal: bool, scale: float, rows=None,
     if return_probs:
         return o, lse, p.reshape(lead + (n_rows, Nk))
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0,
+                  dtype: str = "bf16"):
+    """Exact gradients of the attention forward, in fp64.
+
+    q, k, v, dout: uint16 bit patterns (``dtype`` "bf16" or "f16") shaped
+    ``[..., N, d]`` (square attention; causal: query i sees keys 0..i).
+    Returns ``(dQ, dK, dV)`` as fp64 arrays of the same shape: the gradients
+    of ``sum(dout * O)`` with respect to Q, K and V, from the softmax
+    Jacobian written out (no tiling).
+    """
+    lib = _load()
+    q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
+    if not (q.shape == k.shape == v.shape == dout.shape):
+        raise ValueError("q, k, v and dout must share the shape [..., N, d]")
+    if dtype not in _FORMATS:
+        raise ValueError(f"dtype must be one of {sorted(_FORMATS)}")
+    N, d = q.shape[-2:]
+    BH = int(np.prod(q.shape[:-2])) if q.ndim > 2 else 1
+    dq, dk, dv = (np.empty(q.shape, dtype=np.float64) for _ in range(3))
+    rc = lib.oracle_attention_bwd(_ptr(q, _u16p), _ptr(k, _u16p), _ptr(v, _u16p),
+                                  _ptr(dout, _u16p), BH, N, d, int(bool(causal)), float(scale),
+                                  _ptr(dq, _f64p), _ptr(dk, _f64p), _ptr(dv, _f64p),
+                                  int(threads), _FORMATS[dtype])
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd failed with code {rc}")
+    return dq, dk, dv

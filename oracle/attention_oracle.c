@@ -229,6 +229,83 @@ int oracle_attention_rect_fmt(const uint16_t *q, const uint16_t *k, const uint16
     return failed ? -2 : 0;
 }
 
+/*
+ * Gradients of the attention forward (the backward pass by recomputation
+ * that "Parsing FlashAttention (2)" §1 and "Online Softmax and
+ * FlashAttention" name as the reason to keep the row statistics), written
+ * from the definition rather than any tiling: for every query row i, with
+ * s_ij the scaled, masked scores and P_ij = softmax_j(s_ij),
+ *   dV_j  += P_ij dO_i                       (O = P V)
+ *   dP_ij  = dO_i . V_j
+ *   dS_ij  = P_ij (dP_ij - sum_k P_ik dP_ik)  (Jacobian of a softmax row)
+ *   dQ_i   = scale * sum_j dS_ij K_j          (s = scale * Q K^T)
+ *   dK_j  += scale * dS_ij Q_i.
+ *   q, k, v, dout : [BH][N][d] 16-bit patterns of format fmt
+ *   dq, dk, dv    : [BH][N][d] fp64, written
+ * Square attention (causal: query i sees keys 0..i).  One (batch, head)
+ * slice per OpenMP task.  Returns 0, -1 on bad arguments, -2 on allocation
+ * failure.
+ */
+int oracle_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int64_t BH, int64_t N, int64_t d, int causal,
+                         double scale, double *dq, double *dk, double *dv, int n_threads,
+                         int fmt)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
+    if (BH <= 0 || N <= 0 || d <= 0) return -1;
+    if (fmt != ORACLE_BF16 && fmt != ORACLE_F16) return -1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const uint16_t *qh = q + bh * N * d, *kh = k + bh * N * d;
+        const uint16_t *vh = v + bh * N * d, *doh = dout + bh * N * d;
+        double *dqh = dq + bh * N * d, *dkh = dk + bh * N * d, *dvh = dv + bh * N * d;
+        double *s = (double *)malloc((size_t)N * sizeof(double));
+        double *p = (double *)malloc((size_t)N * sizeof(double));
+        double *dp = (double *)malloc((size_t)N * sizeof(double));
+        if (!s || !p || !dp) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+            free(s);
+            free(p);
+            free(dp);
+            continue;
+        }
+        for (int64_t x = 0; x < N * d; ++x) dkh[x] = dvh[x] = 0.0;
+        for (int64_t i = 0; i < N; ++i) {
+            score_row_fmt(qh + i * d, kh, i, N, d, scale, causal, fmt, s);
+            oracle_safe_softmax(s, N, NULL, p, NULL, NULL);
+            double pdp = 0.0; /* sum_k P_ik dP_ik */
+            for (int64_t j = 0; j < N; ++j) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < d; ++t)
+                    acc += widen(doh[i * d + t], fmt) * widen(vh[j * d + t], fmt);
+                dp[j] = acc;
+                pdp += p[j] * acc;
+            }
+            for (int64_t t = 0; t < d; ++t) dqh[i * d + t] = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                if (p[j] == 0.0) continue; /* masked: P = 0 and dS = 0 */
+                double ds = p[j] * (dp[j] - pdp);
+                for (int64_t t = 0; t < d; ++t) {
+                    dvh[j * d + t] += p[j] * widen(doh[i * d + t], fmt);
+                    dqh[i * d + t] += scale * ds * widen(kh[j * d + t], fmt);
+                    dkh[j * d + t] += scale * ds * widen(qh[i * d + t], fmt);
+                }
+            }
+        }
+        free(s);
+        free(p);
+        free(dp);
+    }
+    return failed ? -2 : 0;
+}
+
 /* oracle_attention_rect_fmt on bf16 inputs. */
 int oracle_attention_rect(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                           int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
