@@ -41,6 +41,9 @@ UNIT = "TFLOPS"
 # The split-KV decode workloads are bound by HBM: GB/s of algorithmic bytes.
 DECODE_METRIC = "split-KV decode attention GB/s of algorithmic HBM bytes & % of measured HBM bandwidth"
 DECODE_UNIT = "GB/s"
+# The backward pass: nominal FLOPs are 2.5x the forward's (five N x N x d
+# products against two), the convention of the FlashAttention line of work.
+BWD_METRIC = "attention bwd TFLOPS (nominal 2.5x forward FLOPs) & % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) of one split-pass launch, from one ncu capture
@@ -446,6 +449,172 @@ def run_ours(args, w):
     return 0
 
 
+def run_reference_bwd(args, w):
+    """The oracle's backward on one (batch, head) slice of the workload per
+    step (one slice runs on one thread); rank 0 only."""
+    import oracle
+
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    q, k, v = workloads.generate(w)
+    do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=5000 + w.seed)[0]
+    sl = [np.ascontiguousarray(a[:1, :1]) for a in (q, k, v, do)]
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.attention_bwd(*sl, w.causal, w.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    fl = 2.5 * w.flops / (w.B * w.H)
+    value = fl * len(times) / total / 1e12
+    sample = f"gradients of 1 of the {w.B * w.H} (batch, head) slices per step, fp64 oracle, 1 thread"
+    print(json.dumps({
+        "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0}), flush=True)
+    return 0
+
+
+def run_ours_bwd(args, w):
+    """Time fa_bwd (pre-pass, dK/dV pass, dQ pass) on the workload's shape;
+    O and LSE come from one untimed fa_fwd, dO is seeded."""
+    import torch
+
+    import tiled_attention_forward_attn_gb300 as fa
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load_library()
+    q, k, v = workloads.generate(w)
+    do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=5000 + w.seed)[0]
+    qd, kd, vd, dod = (workloads.as_torch(a).to(dev) for a in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, w.causal, w.scale, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_stop()
+    if world > 1:
+        torch.distributed.barrier()
+    per_launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    kernel_ms = sum(per_launch_ms)
+    clocks = sampler.stop() if sampler else None
+
+    # End to end: Q, K, V, O, LSE, dO in from pinned host memory, dQ, dK, dV out.
+    hosts_in = [workloads.as_torch(a).pin_memory() for a in (q, k, v)]
+    hosts_in += [o.cpu().pin_memory(), lse.cpu().pin_memory(), workloads.as_torch(do).pin_memory()]
+    devs_in = [qd, kd, vd, o, lse, dod]
+    hosts_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in hosts_in)
+    d2h = sum(t.numel() * t.element_size() for t in hosts_out)
+
+    def e2e_step():
+        for dst, src in zip(devs_in, hosts_in):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(hosts_out, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(10, min(args.steps, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    kernel_ms, e2e_ms = reduce_max_over_ranks([kernel_ms, e2e_ms], device=dev)
+
+    if rank == 0:
+        import oracle
+
+        peaks, peaks_src = load_peaks()
+        flops_step = 2.5 * w.flops
+        value = job_tflops(world, flops_step, args.steps, kernel_ms)
+        achieved = flops_step / (kernel_ms * 1e-3 / args.steps) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        cpu = None
+        if world == 1 and not args.skip_cpu_baseline:
+            sl = [np.ascontiguousarray(a[:1, :1]) for a in (q, k, v, do)]
+            t0 = time.perf_counter()
+            oracle.attention_bwd(*sl, w.causal, w.scale)
+            dt = time.perf_counter() - t0
+            cpu = {"value": 2.5 * w.flops / (w.B * w.H) / dt / 1e12, "unit": UNIT,
+                   "cores": 1, "kind": "oracle",
+                   "sample": (f"gradients of one of the {w.B * w.H} (batch, head) slices, fp64 "
+                              f"oracle (one slice runs on one thread), {dt:.1f} s")}
+        line = {
+            "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "scale": w.scale,
+                       "l2": "flushed between launches (256 MiB write, untimed)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_source": f"{peaks_src} bf16_tflops (burst)",
+                         "timed": "pre-pass, dK/dV pass and dQ pass together, per step",
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": job_tflops(world, flops_step, e2e_steps, e2e_ms), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": 3 * args.steps,
+            "launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
+                          "max": max(per_launch_ms)},
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -460,10 +629,18 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="query rows per head per step of --impl reference")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=("fwd", "bwd"), default="fwd",
+                    help="bwd: time the backward pass of the (square) workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = workloads.by_name(args.workload)
+    if args.pass_ == "bwd":
+        if not isinstance(w, workloads.Workload) or w.dtype != "bf16" or w.d not in (64, 128):
+            ap.error("--pass bwd takes a bf16 square workload with d = 64 or 128")
+        if args.impl == "reference":
+            return run_reference_bwd(args, w)
+        return run_ours_bwd(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -181,6 +181,37 @@ int fa_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o, 
 /* Size in bytes of fa_fwd_splitkv_static's built-in scratch array. */
 size_t fa_fwd_splitkv_static_scratch_bytes(void);
 
+/*
+ * fa_bwd — gradients of the attention forward: the backward pass by
+ * recomputation for which "Parsing FlashAttention (2)" §1 and "Online
+ * Softmax and FlashAttention" keep the row statistics (here LSE).
+ *
+ * With s = scale * Q K^T (+ causal mask), P = exp(s - LSE), D_i =
+ * rowsum(dO_i * O_i):  dV = P^T dO,  dS = P * (dO V^T - D),
+ * dQ = scale * dS K,  dK = scale * dS^T Q  (the gradients of sum(dO * O)).
+ *
+ *   q, k, v, o, dout : const bf16 [B][H][N][d] (device, contiguous, 16-byte
+ *                      aligned); o and lse as written by fa_fwd for the same
+ *                      q, k, v, causal and scale
+ *   lse              : const fp32 [B][H][N] (device, 4-byte aligned)
+ *   dq, dk, dv       : bf16 [B][H][N][d] (device), written
+ *   d                : 64 or 128;  causal, scale as for fa_fwd
+ *   workspace        : device scratch of at least fa_bwd_workspace_bytes()
+ *                      bytes (16-byte aligned), owned by the caller,
+ *                      overwritten (D and LSE * log2(e) per query row)
+ * Outputs and workspace must not overlap an input or each other.  Three
+ * kernel launches on `stream` (a pre-pass, the dK/dV pass, the dQ pass), no
+ * atomics: the result is deterministic.  Returns FA_OK or an FA_ERR_* code
+ * (FA_ERR_WORKSPACE when the workspace is missing or small); validates
+ * before enqueueing; asynchronous.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+           int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes fa_bwd needs (0 on invalid arguments). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
 /* Human-readable text for a return code (static storage, never NULL). */
 const char *fa_strerror(int code);
 

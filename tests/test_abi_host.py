@@ -219,3 +219,33 @@ def test_splitkv_without_device_reports_an_error(lib):
         pytest.skip("a device is present; covered by the GPU tests")
     assert _split(lib) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
     assert lib.fa_fwd_splitkv_num_splits(1, 1, 1, 1000, 64, 0) == 0  # needs the device
+
+
+def test_bwd_validation(lib):
+    import torch
+
+    big = 1 << 24
+    args = dict(q=big, k=2 * big, v=3 * big, o=4 * big, lse=5 * big, do=6 * big, dq=7 * big,
+                dk=8 * big, dv=9 * big, B=1, H=2, N=300, d=64, causal=1, scale=0.1,
+                ws=10 * big, ws_bytes=1 << 20)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                          a["dv"], a["B"], a["H"], a["N"], a["d"], a["causal"], a["scale"],
+                          a["ws"], a["ws_bytes"], None)
+
+    # 2 rows of D and LSE*log2(e) per head, padded to 384 rows: 2 * 2 * 384 * 4 bytes
+    assert lib.fa_bwd_workspace_bytes(1, 2, 300, 64) == 6144
+    assert lib.fa_bwd_workspace_bytes(1, 2, 300, 96) == 0
+    assert call(q=0) == FA_ERR_NULL
+    assert call(d=96) == FA_ERR_HEAD_DIM
+    assert call(N=0) == FA_ERR_SHAPE
+    assert call(dk=8 * big + 8) == FA_ERR_ALIGN
+    assert call(scale=float("nan")) == FA_ERR_SCALE
+    assert call(ws_bytes=6000) == FA_ERR_WORKSPACE
+    assert call(dq=big) == FA_ERR_ALIAS            # dq over q
+    assert call(dv=8 * big + 64) == FA_ERR_ALIAS   # dv inside dk
+    assert call(ws=9 * big) == FA_ERR_ALIAS        # workspace over dv
+    if not torch.cuda.is_available():
+        assert call() in (FA_ERR_LAUNCH, FA_ERR_DEVICE)

@@ -1,0 +1,103 @@
+"""GPU parity of the backward pass (fa_bwd, through the C ABI) against the
+fp64 oracle's gradients.
+
+Tolerance, from the arithmetic: the gradients are rounded to bf16 (2^-9
+relative) and are sums over up to N products whose one operand (P or dS)
+is rounded to bf16 before the MMA, accumulated in fp32; dS = P (dP - D)
+also inherits the bf16 rounding of the forward's O through D.  Elementwise
+|dX - ref| <= 3e-2 (1 + |ref|), and the relative Frobenius error of each
+gradient (floored at the norm of an all-ones tensor) <= 1e-2 (observed:
+<= 1.2e-2 elementwise)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+G_ATOL = 3e-2
+G_FRO = 1e-2
+
+
+@pytest.fixture(scope="module")
+def fa(cuda_device):
+    import tiled_attention_forward_attn_gb300 as fa
+    from tiled_attention_forward_attn_gb300 import _build
+
+    _build.build()
+    fa.load_library()
+    return fa
+
+
+def _grads(fa, dev, q, k, v, do, causal, scale):
+    import torch
+
+    qd, kd, vd, dod = (workloads.as_torch(a).to(dev) for a in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize(dev)
+    assert fa.fa_get_device_status() == 0
+    return [t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+
+
+def check_grads(got, ref, label):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert g.shape == r.shape
+        assert np.all(np.isfinite(g)), f"{label} {name}: non-finite"
+        err = np.abs(g - r)
+        worst = float((err / (1.0 + np.abs(r))).max())
+        # relative to the reference's norm, floored at that of an all-ones
+        # tensor (as the elementwise bound uses 1 + |ref|): with one key,
+        # dQ and dK are exactly 0.
+        fro = float(np.linalg.norm(err) / max(np.linalg.norm(r), math.sqrt(r.size)))
+        assert worst <= G_ATOL, f"{label} {name}: max |d|/(1+|ref|) = {worst:.3e}"
+        assert fro <= G_FRO, f"{label} {name}: relative Frobenius error {fro:.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 17, 128, 129, 300, 1000])
+def test_bwd_matches_oracle(fa, cuda_device, N, d, causal):
+    q, k, v = workloads.generate_shape(1, 2, N, d, seed=1000 + N + d, qk_std=1.5)
+    do = workloads.generate_shape(1, 2, N, d, seed=1100 + N + d)[0]
+    scale = 1.0 / math.sqrt(d)
+    got = _grads(fa, cuda_device, q, k, v, do, causal, scale)
+    ref = oracle.attention_bwd(q, k, v, do, causal, scale)
+    check_grads(got, ref, f"N{N} d{d} c{causal}")
+
+
+def test_bwd_headline_shape_on_four_heads(fa, cuda_device):
+    """B=2, H=16, N=4096, d=128, causal: the GPU computes every head; four
+    heads (two per batch) are checked against the oracle in full."""
+    w = workloads.HEADLINE
+    q, k, v = workloads.generate(w)
+    do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=1200)[0]
+    got = _grads(fa, cuda_device, q, k, v, do, w.causal, w.scale)
+    heads = [(0, 0), (0, 9), (1, 4), (1, 15)]
+
+    def pick(a):
+        return np.stack([a[b, h] for b, h in heads])[None]
+
+    ref = oracle.attention_bwd(pick(q), pick(k), pick(v), pick(do), w.causal, w.scale)
+    check_grads([pick(g) for g in got], ref, w.name)
+
+
+def test_bwd_deterministic_and_workspace_checked(fa, cuda_device):
+    import torch
+
+    q, k, v = workloads.generate_shape(2, 2, 500, 64, seed=1300)
+    do = workloads.generate_shape(2, 2, 500, 64, seed=1301)[0]
+    a = _grads(fa, cuda_device, q, k, v, do, True, 0.1)
+    b = _grads(fa, cuda_device, q, k, v, do, True, 0.1)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    qd = workloads.as_torch(q).to(cuda_device)
+    o, lse = fa.attention_forward(qd, qd, qd, causal=False, scale=0.1)
+    grads = [torch.empty_like(qd) for _ in range(3)]
+    small = torch.empty(fa.fa_bwd_workspace_bytes(2, 2, 500, 64) - 16, dtype=torch.uint8,
+                        device=cuda_device)
+    with pytest.raises(fa.FAError) as err:
+        fa.fa_bwd(qd, qd, qd, o, lse, qd, *grads, False, 0.1, small)
+    assert err.value.code == 10

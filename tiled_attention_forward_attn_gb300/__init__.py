@@ -20,6 +20,7 @@ __all__ = [
     "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version", "fa_fwd_strided",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
+    "fa_bwd", "fa_bwd_workspace_bytes", "attention_backward",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
     "fa_set_fault_injection", "load_library", "LIB_PATH",
     "FA_DEVICE_STATUS_TIMEOUT", "FA_INJECT_SKIP_FIRST_V_LOAD",
@@ -79,6 +80,11 @@ def load_library(path: str | None = None):
         lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.fa_fwd_splitkv_num_splits.restype = i
         lib.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
+        lib.fa_bwd.restype = i
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
+                               ctypes.c_size_t, vp]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_fwd_splitkv_static.restype = i
         lib.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_splitkv_static_scratch_bytes.restype = ctypes.c_size_t
@@ -292,6 +298,66 @@ def fa_fwd_splitkv_static(q, k, v, o, lse, causal: bool, scale: float, num_split
             q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
             d, int(bool(causal)), float(scale), int(num_splits), handle or None)
         _check(rc, "fa_fwd_splitkv_static")
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Workspace bytes fa_bwd needs (0 on invalid arguments)."""
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, workspace=None,
+           stream=None) -> None:
+    """Attention backward into preallocated CUDA tensors.
+
+    q, k, v, o, dout, dq, dk, dv: contiguous ``torch.bfloat16`` ``[B, H, N, d]``
+    on one device; lse: ``torch.float32`` ``[B, H, N]`` (o and lse from
+    :func:`fa_fwd`).  ``workspace``: a CUDA byte tensor of at least
+    :func:`fa_bwd_workspace_bytes`; allocated here when None.
+    """
+    import torch
+
+    B, H, N, d = _dims(q)
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
+                    ("dv", dv)):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(B, H, N, d)}")
+    if tuple(lse.shape) != (B, H, N):
+        raise ValueError(f"lse has shape {tuple(lse.shape)}, expected {(B, H, N)}")
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
+                        ("dout", dout, torch.bfloat16), ("dq", dq, torch.bfloat16),
+                        ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor on q's device")
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            nbytes = fa_bwd_workspace_bytes(B, H, N, d)
+            if nbytes == 0:
+                raise FAError(3, "fa_bwd_workspace_bytes")
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        rc = load_library().fa_bwd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+            int(bool(causal)), float(scale), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), handle or None)
+        _check(rc, "fa_bwd")
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+                       stream=None):
+    """Allocate dQ, dK, dV and run :func:`fa_bwd`; returns ``(dQ, dK, dV)``."""
+    import torch
+
+    d = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, None, stream)
+    return dq, dk, dv
 
 
 def fa_get_device_status() -> int:

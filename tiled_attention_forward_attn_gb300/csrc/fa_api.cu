@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_splitkv.cuh"
 
@@ -67,6 +68,12 @@ bool configure_dim() {
          configure_both_signs<D, false, true>() && configure_both_signs<D, true, true>();
 }
 
+template <int D, bool kKV>
+cudaError_t configure_bwd_kernel() {
+  return cudaFuncSetAttribute(fa::fa_bwd_kernel<D, kKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::BwdCfg<D, kKV>::kSmemAlloc));
+}
+
 template <int D>
 cudaError_t configure_split_kernel() {
   return cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D>,
@@ -98,7 +105,11 @@ int prepare_device(int* dev_out, int* sms_out) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
   if (!configure_dim<64>() || !configure_dim<128>() ||
-      configure_split_kernel<64>() != cudaSuccess || configure_split_kernel<128>() != cudaSuccess)
+      configure_split_kernel<64>() != cudaSuccess || configure_split_kernel<128>() != cudaSuccess ||
+      configure_bwd_kernel<64, true>() != cudaSuccess ||
+      configure_bwd_kernel<64, false>() != cudaSuccess ||
+      configure_bwd_kernel<128, true>() != cudaSuccess ||
+      configure_bwd_kernel<128, false>() != cudaSuccess)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
   *sms_out = sms;
@@ -304,6 +315,108 @@ extern "C" int fa_fwd_strided(const void* q, const int64_t* q_strides, const voi
                               int H, int N, int d, int causal, float scale, void* stream) {
   return fwd_impl(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, dtype, B, H, N, d,
                   causal, scale, stream);
+}
+
+// ---------------------------------------------------------------- backward
+
+namespace {
+
+int64_t bwd_npad(int N) { return (static_cast<int64_t>(N) + fa::kBwdTile - 1) / fa::kBwdTile * fa::kBwdTile; }
+
+// Three launches on one stream: D and LSE*log2(e) into the workspace, the
+// dK/dV pass (prm_kv: out0 = dK, out1 = dV), the dQ pass (prm_q: out0 = dQ).
+template <int D>
+int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensorMap& mq,
+               const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+               const fa::BwdParams& base, const fa::BwdParams& prm_q, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(base.num_bh) * base.Npad;
+  const int64_t threads = rows * (D / 8);  // a multiple of 256: Npad is a multiple of 128
+  fa::fa_bwd_prep_kernel<D><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
+      const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  const unsigned ctas = static_cast<unsigned>(static_cast<int64_t>(base.T) * base.num_bh);
+  fa::fa_bwd_kernel<D, true><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, true>::kSmemAlloc, stream>>>(
+      mk, mv, mq, mdo, base);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa::fa_bwd_kernel<D, false><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, false>::kSmemAlloc, stream>>>(
+      mq, mdo, mk, mv, prm_q);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  return static_cast<size_t>(2 * BH * bwd_npad(N) * 4);
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                      int causal, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1)) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t Npad = bwd_npad(N);
+  const int64_t T = Npad / fa::kBwdTile;
+  if (BH > INT_MAX || BH * T > INT_MAX || BH * Npad > INT_MAX) return FA_ERR_SHAPE;
+  for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv),
+                          static_cast<const void*>(workspace)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  const size_t tb = static_cast<size_t>(BH) * N * d * 2;
+  const size_t lb = static_cast<size_t>(BH) * N * 4;
+  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  // Outputs (dq, dk, dv, workspace) overlap neither an input nor each other.
+  const void* ins[6] = {q, k, v, o, lse, dout};
+  const size_t in_bytes[6] = {tb, tb, tb, tb, lb, tb};
+  const void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_bytes[4] = {tb, tb, tb, need};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA_ERR_ALIAS;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_ALIAS;
+  }
+
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
+  if (prep != FA_OK) return prep;
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
+      !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
+      !encode_map(&mv, v, static_cast<int>(BH), N, d) ||
+      !encode_map(&mdo, dout, static_cast<int>(BH), N, d))
+    return FA_ERR_LAUNCH;
+
+  fa::BwdParams prm;
+  prm.out0 = static_cast<uint16_t*>(dk);
+  prm.out1 = static_cast<uint16_t*>(dv);
+  float* ws = static_cast<float*>(workspace);
+  prm.lse2 = ws;
+  prm.dvec = ws + BH * Npad;
+  prm.N = N;
+  prm.Npad = static_cast<int>(Npad);
+  prm.T = static_cast<int>(T);
+  prm.num_bh = static_cast<int>(BH);
+  prm.causal = causal;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.scale = scale;
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  fa::BwdParams prm_q = prm;
+  prm_q.out0 = static_cast<uint16_t*>(dq);
+  prm_q.out1 = nullptr;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_bwd<64>(o, dout, lse, mq, mk, mv, mdo, prm, prm_q, st)
+                 : launch_bwd<128>(o, dout, lse, mq, mk, mv, mdo, prm, prm_q, st);
 }
 
 // ---------------------------------------------------------------- split-KV

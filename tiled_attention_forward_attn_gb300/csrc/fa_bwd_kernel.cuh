@@ -1,0 +1,415 @@
+// Attention backward by recomputation for sm_103a.
+//
+// Given Q, K, V, the forward's O and LSE and the output gradient dO, the
+// gradients of sum(dO * O) are, with s = scale * Q K^T (+ causal mask),
+// P = exp(s - LSE) (the forward's probabilities, recomputed from the saved
+// row statistic as "Parsing FlashAttention (2)" §1 and "Online Softmax and
+// FlashAttention" keep it for), D_i = rowsum(dO_i * O_i):
+//     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),
+//     dQ = scale * dS K,   dK = scale * dS^T Q.
+// (D_i equals sum_j P_ij dP_ij, the softmax Jacobian's correction term,
+// because O = P V.)
+//
+// Three launches, no atomics:
+//   fa_bwd_prep_kernel    D and LSE * log2(e) per query row, into a
+//                         workspace padded to whole 128-row tiles;
+//   fa_bwd_kernel<D,true> one CTA per (batch*head, 128-key tile j): K_j and
+//                         V_j stay in shared memory, Q_i, dO_i and the
+//                         tile's D, LSE stream through a TMA ring; per query
+//                         tile i the tensor core computes S^T = K_j Q_i^T
+//                         and dP^T = V_j dO_i^T into TMEM, four warps (one
+//                         key row = one TMEM lane each) turn them into P^T
+//                         and dS^T (bf16 pairs written back over them), and
+//                         dV_j += P^T dO_i, dK_j += dS^T Q_i accumulate in
+//                         TMEM with P^T / dS^T read straight from TMEM;
+//   fa_bwd_kernel<D,false> one CTA per (batch*head, 128-query tile i): Q_i
+//                         and dO_i stay, K_j and V_j stream; S, dP into
+//                         TMEM, dS written back over S, dQ_i += dS K_j.
+// Causal: the key tile j only meets query tiles i >= j, the query tile i
+// only key tiles j <= i; the diagonal tile is masked element by element.
+//
+// TMEM (512 columns): S [0,128), dP [128,256), then the accumulators (dK and
+// dV, or dQ), D columns each.  Warps: 0-3 elementwise and epilogue, 4 the
+// TMA producer, 5 the TMEM allocator and MMA issuer.  Every wait is bounded
+// like the forward's (status word, drain, TMEM freed).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <math_constants.h>
+
+#include "fa_fwd_kernel.cuh"  // wait helpers, status word, kSwBlockBytes
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdLoadWarp = 4;
+constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdTile = 128;  // rows of every tile (keys or queries)
+
+struct BwdParams {
+  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][D] bf16
+  uint16_t* out1;     // key-tile pass: dV; unused otherwise
+  const float* lse2;  // [BH][Npad] LSE * log2(e) per query (0 past N)
+  const float* dvec;  // [BH][Npad] rowsum(dO * O) per query (0 past N)
+  int N;              // sequence length
+  int Npad;           // N rounded up to whole tiles
+  int T;              // tiles per (batch, head) = Npad / 128
+  int num_bh;         // B * H
+  int causal;
+  float scale_log2;   // scale * log2(e)
+  float scale;        // the softmax scale
+  uint64_t wait_limit_ns;
+};
+
+template <int D, bool kKV>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr uint32_t kTileBytes = kBwdTile * D * 2;
+  static constexpr uint32_t kVecBytes = kKV ? 1024 : 0;  // LSE2[128] then D[128], fp32
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes + kVecBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the swizzle");
+  static constexpr uint32_t kOffX = 0;                // stationary tiles X0, X1
+  static constexpr uint32_t kOffY = 2 * kTileBytes;   // ring of (Y0, Y1[, vectors])
+  static constexpr uint32_t kOffBar = kOffY + kStages * kStageBytes;
+  // x_full, st_full, p_full, acc_done, y_full[S], y_empty[S]
+  static constexpr int kNumBars = 4 + 2 * kStages;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr uint32_t kSmemBytes = kOffMisc + 16;
+  static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+  static_assert(kSmemAlloc <= 232448, "dynamic shared memory per block");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;      // S / S^T; then P^T or dS as bf16 pairs
+  static constexpr uint32_t kColDP = 128;   // dP / dP^T; then dS^T (key-tile pass)
+  static constexpr uint32_t kColAcc0 = 256;      // dK (key-tile pass) or dQ
+  static constexpr uint32_t kColAcc1 = 256 + D;  // dV (key-tile pass)
+};
+
+struct BwdBars {
+  uint32_t base;
+  int stages;
+  __device__ uint32_t x_full() const { return base; }
+  __device__ uint32_t st_full() const { return base + 8u; }
+  __device__ uint32_t p_full() const { return base + 16u; }
+  __device__ uint32_t acc_done() const { return base + 24u; }
+  __device__ uint32_t y_full(int s) const { return base + 32u + 8u * s; }
+  __device__ uint32_t y_empty(int s) const { return base + 32u + 8u * (stages + s); }
+};
+
+// D_i = rowsum(dO_i * O_i) and LSE_i * log2(e) for every row of the padded
+// [BH][Npad] layout (0 past N).  D/8 threads per row, 16 bytes each.
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                       const float* __restrict__ lse, float* __restrict__ lse2,
+                       float* __restrict__ dvec, int N, int Npad) {
+  constexpr int kTpr = D / 8;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gid / kTpr;  // padded row index bh * Npad + n
+  const int part = static_cast<int>(gid % kTpr);
+  const int64_t bh = row / Npad;
+  const int n = static_cast<int>(row - bh * Npad);
+  float acc = 0.0f;
+  if (n < N) {
+    const size_t off = (static_cast<size_t>(bh) * N + n) * D + part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (part == 0) {
+    dvec[row] = n < N ? acc : 0.0f;
+    lse2[row] = n < N ? lse[static_cast<size_t>(bh) * N + n] * 1.4426950408889634f : 0.0f;
+  }
+}
+
+// kKV = true: X = (K, V) of key tile xt, Y = (Q, dO) of query tiles.
+// kKV = false: X = (Q, dO) of query tile xt, Y = (K, V) of key tiles.
+template <int D, bool kKV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
+                  const __grid_constant__ CUtensorMap tm_y0, const __grid_constant__ CUtensorMap tm_y1,
+                  const BwdParams p) {
+  using C = BwdCfg<D, kKV>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sX = sbase + C::kOffX;
+  const uint32_t sY = sbase + C::kOffY;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+  const BwdBars bars{sbase + C::kOffBar, S};
+  const WaitCtx wctx{abort_flag, p.wait_limit_ns};
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Tile of this CTA, heaviest first under the causal mask: key tile 0 meets
+  // every query tile; query tile T-1 meets every key tile.
+  const int band = static_cast<int>(blockIdx.x) / p.num_bh;
+  const int bh = static_cast<int>(blockIdx.x) - band * p.num_bh;
+  const int xt = kKV ? band : p.T - 1 - band;
+  const int y_first = (kKV && p.causal) ? xt : 0;
+  const int y_last = (!kKV && p.causal) ? xt : p.T - 1;
+  const int steps = y_last - y_first + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars.x_full(), 1);
+    mbar_init(bars.st_full(), 1);
+    mbar_init(bars.p_full(), 4);  // one arrival per elementwise warp
+    mbar_init(bars.acc_done(), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars.y_full(s), 1);
+      mbar_init(bars.y_empty(s), 1);
+    }
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  if (warp == kBwdLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tm_x0);
+    tma_prefetch_desc(&tm_x1);
+    tma_prefetch_desc(&tm_y0);
+    tma_prefetch_desc(&tm_y1);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ elementwise
+    const int row = threadIdx.x;  // = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
+    const float cs = p.scale_log2;
+    float lse2_r = 0.0f, d_r = 0.0f;
+    if (!kKV) {
+      lse2_r = p.lse2[static_cast<size_t>(bh) * p.Npad + x_idx];
+      d_r = p.dvec[static_cast<size_t>(bh) * p.Npad + x_idx];
+    }
+    bool ok = true;
+    for (int n = 0; n < steps; ++n) {
+      if (!warp_wait_bar(bars.st_full(), parity_of(n), wctx)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int yt = y_first + n;
+      const int y0 = yt * kBwdTile;
+      const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdTile > p.N);
+      const float* vec = reinterpret_cast<const float*>(
+          smem + C::kOffY + (n % S) * C::kStageBytes + 2 * C::kTileBytes);
+#pragma unroll
+      for (int cc = 0; cc < kBwdTile / 32; ++cc) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_off + C::kColS + 32 * cc, sr);
+        tmem_ld32(tmem + lane_off + C::kColDP + 32 * cc, dr);
+        tmem_ld_wait();
+        tmem_ld_fence(sr);
+        tmem_ld_fence(dr);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pe[2], de[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 32 * cc + e + h;
+            const float lse2 = kKV ? vec[c] : lse2_r;
+            const float dd = kKV ? vec[kBwdTile + c] : d_r;
+            float pv = ex2_approx(__uint_as_float(sr[e + h]) * cs - lse2);
+            if (need_mask) {
+              const int y_idx = y0 + c;
+              // key <= query when causal; padding rows past N see nothing.
+              const bool vis = y_idx < p.N &&
+                               (!p.causal || (kKV ? x_idx <= y_idx : y_idx <= x_idx));
+              if (!vis) pv = 0.0f;
+            }
+            pe[h] = pv;
+            de[h] = pv * (__uint_as_float(dr[e + h]) - dd);
+          }
+          pp[e / 2] = pack_bf16x2(pe[0], pe[1]);
+          pd[e / 2] = pack_bf16x2(de[0], de[1]);
+        }
+        // Packed pairs of chunk cc land in columns [16cc, 16cc + 16), which
+        // this chunk has already read.
+        if (kKV) {
+          tmem_st16(tmem + lane_off + C::kColS + 16 * cc, pp);
+          tmem_st16(tmem + lane_off + C::kColDP + 16 * cc, pd);
+        } else {
+          tmem_st16(tmem + lane_off + C::kColS + 16 * cc, pd);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.p_full());
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok && warp_wait_bar(bars.acc_done(), 0, wctx)) {
+      tc_fence_after_sync();
+      const bool in_range = x_idx < p.N;
+#pragma unroll
+      for (int a = 0; a < (kKV ? 2 : 1); ++a) {
+        // kKV: a = 0 -> dK (scaled), a = 1 -> dV; otherwise dQ (scaled).
+        const uint32_t col = a == 0 ? C::kColAcc0 : C::kColAcc1;
+        const float mul = a == 0 ? p.scale : 1.0f;
+        uint16_t* out = a == 0 ? p.out0 : p.out1;
+        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + col + 32 * cc, r);
+          tmem_ld_wait();
+          tmem_ld_fence(r);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack_bf16x2(__uint_as_float(r[8 * g + 2 * e]) * mul,
+                                  __uint_as_float(r[8 * g + 2 * e + 1]) * mul);
+            if (in_range) dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+    }
+  } else if (warp == kBwdLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      // Y tiles are read by every X tile of the same head: keep them in L2.
+      const uint64_t keep = make_l2_policy_evict_last();
+      const uint64_t once = make_l2_policy_evict_first();
+      mbar_arrive_expect_tx(bars.x_full(), 2 * C::kTileBytes);
+#pragma unroll
+      for (int b = 0; b < D / 64; ++b) {
+        tma_load_3d_hint(sX + b * kSwBlockBytes, &tm_x0, bars.x_full(), 64 * b, xt * kBwdTile, bh,
+                         once);
+        tma_load_3d_hint(sX + C::kTileBytes + b * kSwBlockBytes, &tm_x1, bars.x_full(), 64 * b,
+                         xt * kBwdTile, bh, once);
+      }
+      int issued = 0;
+      for (int n = 0; n < steps; ++n) {
+        const int s = n % S;
+        if (n >= S && !wait_bar(bars.y_empty(s), parity_of(n / S - 1), wctx)) break;
+        const int yt = y_first + n;
+        const uint32_t stage = sY + s * C::kStageBytes;
+        mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_3d_hint(stage + b * kSwBlockBytes, &tm_y0, bars.y_full(s), 64 * b,
+                           yt * kBwdTile, bh, keep);
+          tma_load_3d_hint(stage + C::kTileBytes + b * kSwBlockBytes, &tm_y1, bars.y_full(s),
+                           64 * b, yt * kBwdTile, bh, keep);
+        }
+        if (kKV) {
+          const size_t v0 = static_cast<size_t>(bh) * p.Npad + yt * kBwdTile;
+          bulk_load(stage + 2 * C::kTileBytes, p.lse2 + v0, kBwdTile * 4, bars.y_full(s));
+          bulk_load(stage + 2 * C::kTileBytes + kBwdTile * 4, p.dvec + v0, kBwdTile * 4,
+                    bars.y_full(s));
+        }
+        issued = n + 1;
+      }
+      // Drain: every copy issued must land before the CTA exits.
+      wait_bar_drain(bars.x_full(), 0, wctx);
+      for (int s = 0; s < S; ++s) {
+        if (issued > s) {
+          const int last = issued - 1 - ((issued - 1 - s) % S);
+          wait_bar_drain(bars.y_full(s), parity_of(last / S), wctx);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = elect_one_sync();
+    constexpr uint32_t kHi = desc_hi_sw128(1024);
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(kBwdTile, kBwdTile, 0, 0);
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBwdTile, D, 0, 1);
+    const uint32_t x_lo = desc_lo(sX, 16);               // X tiles, K-major A
+    const uint32_t yk_lo = desc_lo(sY, 16);              // Y tiles, K-major B
+    const uint32_t ymn_lo = desc_lo(sY, kSwBlockBytes);  // Y tiles, MN-major B
+    auto kmaj_off = [](int kk) -> uint32_t {
+      return ((kk >> 2) * kSwBlockBytes + (kk & 3) * 32) >> 4;
+    };
+    auto commit = [&](uint32_t bar) {
+      if (leader) umma_commit(bar);
+      __syncwarp();
+    };
+    bool ok = warp_wait_bar(bars.x_full(), 0, wctx);
+    for (int n = 0; ok && n < steps; ++n) {
+      const int s = n % S;
+      if (!warp_wait_bar(bars.y_full(s), parity_of(n / S), wctx)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t y0 = (s * C::kStageBytes) >> 4;
+      const uint32_t y1 = (s * C::kStageBytes + C::kTileBytes) >> 4;
+      constexpr uint32_t x1 = C::kTileBytes >> 4;
+      if (leader) {
+        // S = X0 Y0^T and dP = X1 Y1^T over the head dimension.
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_lohi(tmem + C::kColS, x_lo + kmaj_off(kk), kHi, yk_lo + y0 + kmaj_off(kk), kHi,
+                       kIdescSS, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_lohi(tmem + C::kColDP, x_lo + x1 + kmaj_off(kk), kHi, yk_lo + y1 + kmaj_off(kk),
+                       kHi, kIdescSS, kk > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+      commit(bars.st_full());
+      if (!warp_wait_bar(bars.p_full(), parity_of(n), wctx)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (leader) {
+        // Accumulate over the 128 rows of the Y tiles, 16 per MMA; the A
+        // operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM.
+#pragma unroll
+        for (int kk = 0; kk < kBwdTile / 16; ++kk) {
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t yoff = (kk * 16 * 128) >> 4;
+          if (kKV) {
+            umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + 8u * kk, ymn_lo + y1 + yoff, kHi,
+                         kIdescAcc, acc);  // dV += P^T dO
+            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColDP + 8u * kk, ymn_lo + y0 + yoff, kHi,
+                         kIdescAcc, acc);  // dK += dS^T Q
+          } else {
+            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColS + 8u * kk, ymn_lo + y0 + yoff, kHi,
+                         kIdescAcc, acc);  // dQ += dS K
+          }
+        }
+      }
+      __syncwarp();
+      commit(bars.y_empty(s));
+    }
+    // Every MMA issued has completed once acc_done fires.
+    commit(bars.acc_done());
+    wait_bar_drain(bars.acc_done(), 0, wctx);
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa
