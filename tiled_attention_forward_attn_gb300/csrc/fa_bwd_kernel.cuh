@@ -28,10 +28,16 @@
 // Causal: the key tile j only meets query tiles i >= j, the query tile i
 // only key tiles j <= i; the diagonal tile is masked element by element.
 //
-// TMEM (512 columns): S [0,128), dP [128,256), then the accumulators (dK and
-// dV, or dQ), D columns each.  Warps: 0-3 elementwise and epilogue, 4 the
-// TMA producer, 5 the TMEM allocator and MMA issuer.  Every wait is bounded
-// like the forward's (status word, drain, TMEM freed).
+// Each streamed 128-row tile is processed in two 64-row sub-steps whose S
+// and dP live in alternating TMEM buffers, and each buffer has its own
+// warpgroup of elementwise warps: while one warpgroup works on a sub-step,
+// the other works on the next and the tensor core runs the accumulation of
+// the previous one and the S, dP of the one after.  TMEM (512 columns): S
+// buffers [0,64) and [64,128), dP buffers [128,192) and [192,256), then the
+// accumulators (dK and dV, or dQ), D columns each.  Warps: 0-3 and 4-7
+// elementwise (buffer 0 and 1) and epilogue, 8 the TMA producer, 9 the TMEM
+// allocator and MMA issuer.  Every wait is bounded like the forward's
+// (status word, drain, TMEM freed).
 #pragma once
 
 #include <cstdint>
@@ -43,16 +49,17 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdLoadWarp = 4;
-constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdLoadWarp = 8;
+constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdTile = 128;  // rows of every tile (keys or queries)
+constexpr int kBwdSub = 64;    // streamed rows per sub-step
 
 struct BwdParams {
   uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][D] bf16
   uint16_t* out1;     // key-tile pass: dV; unused otherwise
-  const float* lse2;  // [BH][Npad] LSE * log2(e) per query (0 past N)
-  const float* dvec;  // [BH][Npad] rowsum(dO * O) per query (0 past N)
+  const float* lse2;  // [BH][Npad] -LSE * log2(e) per query (0 past N)
+  const float* dvec;  // [BH][Npad] -rowsum(dO * O) per query (0 past N)
   int N;              // sequence length
   int Npad;           // N rounded up to whole tiles
   int T;              // tiles per (batch, head) = Npad / 128
@@ -68,21 +75,21 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int kStages = (D == 64) ? 4 : 2;
   static constexpr uint32_t kTileBytes = kBwdTile * D * 2;
-  static constexpr uint32_t kVecBytes = kKV ? 1024 : 0;  // LSE2[128] then D[128], fp32
+  static constexpr uint32_t kVecBytes = kKV ? 1024 : 0;  // -LSE2[128] then -D[128], fp32
   static constexpr uint32_t kStageBytes = 2 * kTileBytes + kVecBytes;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the swizzle");
   static constexpr uint32_t kOffX = 0;                // stationary tiles X0, X1
   static constexpr uint32_t kOffY = 2 * kTileBytes;   // ring of (Y0, Y1[, vectors])
   static constexpr uint32_t kOffBar = kOffY + kStages * kStageBytes;
-  // x_full, st_full, p_full, acc_done, y_full[S], y_empty[S]
-  static constexpr int kNumBars = 4 + 2 * kStages;
+  // x_full, st_full[2], p_full[2], acc_done, y_full[S], y_empty[S]
+  static constexpr int kNumBars = 6 + 2 * kStages;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "dynamic shared memory per block");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;      // S / S^T; then P^T or dS as bf16 pairs
-  static constexpr uint32_t kColDP = 128;   // dP / dP^T; then dS^T (key-tile pass)
+  static constexpr uint32_t kColS = 0;      // S buffer b at 64b; then P^T or dS as bf16 pairs
+  static constexpr uint32_t kColDP = 128;   // dP buffer b at 128 + 64b; then dS^T (key-tile pass)
   static constexpr uint32_t kColAcc0 = 256;      // dK (key-tile pass) or dQ
   static constexpr uint32_t kColAcc1 = 256 + D;  // dV (key-tile pass)
 };
@@ -91,15 +98,16 @@ struct BwdBars {
   uint32_t base;
   int stages;
   __device__ uint32_t x_full() const { return base; }
-  __device__ uint32_t st_full() const { return base + 8u; }
-  __device__ uint32_t p_full() const { return base + 16u; }
-  __device__ uint32_t acc_done() const { return base + 24u; }
-  __device__ uint32_t y_full(int s) const { return base + 32u + 8u * s; }
-  __device__ uint32_t y_empty(int s) const { return base + 32u + 8u * (stages + s); }
+  __device__ uint32_t st_full(int b) const { return base + 8u + 8u * b; }
+  __device__ uint32_t p_full(int b) const { return base + 24u + 8u * b; }
+  __device__ uint32_t acc_done() const { return base + 40u; }
+  __device__ uint32_t y_full(int s) const { return base + 48u + 8u * s; }
+  __device__ uint32_t y_empty(int s) const { return base + 48u + 8u * (stages + s); }
 };
 
-// D_i = rowsum(dO_i * O_i) and LSE_i * log2(e) for every row of the padded
-// [BH][Npad] layout (0 past N).  D/8 threads per row, 16 bytes each.
+// -D_i = -rowsum(dO_i * O_i) and -LSE_i * log2(e) for every row of the
+// padded [BH][Npad] layout (0 past N), negated for the elementwise pass's
+// fused multiply-adds.  D/8 threads per row, 16 bytes each.
 template <int D>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
@@ -126,8 +134,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (part == 0) {
-    dvec[row] = n < N ? acc : 0.0f;
-    lse2[row] = n < N ? lse[static_cast<size_t>(bh) * N + n] * 1.4426950408889634f : 0.0f;
+    dvec[row] = n < N ? -acc : 0.0f;
+    lse2[row] = n < N ? -lse[static_cast<size_t>(bh) * N + n] * 1.4426950408889634f : 0.0f;
   }
 }
 
@@ -164,8 +172,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bars.x_full(), 1);
-    mbar_init(bars.st_full(), 1);
-    mbar_init(bars.p_full(), 4);  // one arrival per elementwise warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.st_full(b), 1);
+      mbar_init(bars.p_full(b), 4);  // one arrival per warp of buffer b's warpgroup
+    }
     mbar_init(bars.acc_done(), 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.y_full(s), 1);
@@ -189,100 +199,122 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ------------------------------------------------------------ elementwise
-    const int row = threadIdx.x;  // = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = warp >> 2;          // warpgroup = TMEM buffer it serves
+    const int row = threadIdx.x & 127;  // = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
     const float cs = p.scale_log2;
-    float lse2_r = 0.0f, d_r = 0.0f;
+    float nlse_r = 0.0f, nd_r = 0.0f;
     if (!kKV) {
-      lse2_r = p.lse2[static_cast<size_t>(bh) * p.Npad + x_idx];
-      d_r = p.dvec[static_cast<size_t>(bh) * p.Npad + x_idx];
+      nlse_r = p.lse2[static_cast<size_t>(bh) * p.Npad + x_idx];
+      nd_r = p.dvec[static_cast<size_t>(bh) * p.Npad + x_idx];
     }
     bool ok = true;
-    for (int n = 0; n < steps; ++n) {
-      if (!warp_wait_bar(bars.st_full(), parity_of(n), wctx)) {
+    for (int m = g; m < 2 * steps; m += 2) {
+      const int n = m >> 1;
+      if (!warp_wait_bar(bars.st_full(g), parity_of(n), wctx)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       const int yt = y_first + n;
-      const int y0 = yt * kBwdTile;
-      const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdTile > p.N);
-      const float* vec = reinterpret_cast<const float*>(
-          smem + C::kOffY + (n % S) * C::kStageBytes + 2 * C::kTileBytes);
+      const int y0 = yt * kBwdTile + kBwdSub * g;  // first streamed row of this sub-step
+      const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdSub > p.N);
+      const float4* vec = reinterpret_cast<const float4*>(
+          smem + C::kOffY + (n % S) * C::kStageBytes + 2 * C::kTileBytes + 4 * kBwdSub * g);
+      const uint32_t col_s = C::kColS + kBwdSub * g;
+      const uint32_t col_dp = C::kColDP + kBwdSub * g;
 #pragma unroll
-      for (int cc = 0; cc < kBwdTile / 32; ++cc) {
+      for (int cc = 0; cc < kBwdSub / 32; ++cc) {
         uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + C::kColS + 32 * cc, sr);
-        tmem_ld32(tmem + lane_off + C::kColDP + 32 * cc, dr);
+        tmem_ld32(tmem + lane_off + col_s + 32 * cc, sr);
+        tmem_ld32(tmem + lane_off + col_dp + 32 * cc, dr);
         tmem_ld_wait();
         tmem_ld_fence(sr);
         tmem_ld_fence(dr);
         uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pe[2], de[2];
+        for (int e = 0; e < 32; e += 4) {
+          // -LSE2 and -D of the four columns (kKV: per column, from shared
+          // memory; otherwise this row's).
+          float nl[4], nd[4];
+          if (kKV) {
+            const float4 a = vec[(32 * cc + e) / 4];
+            const float4 b = vec[(kBwdTile + 32 * cc + e) / 4];
+            nl[0] = a.x; nl[1] = a.y; nl[2] = a.z; nl[3] = a.w;
+            nd[0] = b.x; nd[1] = b.y; nd[2] = b.z; nd[3] = b.w;
+          } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 32 * cc + e + h;
-            const float lse2 = kKV ? vec[c] : lse2_r;
-            const float dd = kKV ? vec[kBwdTile + c] : d_r;
-            float pv = ex2_approx(__uint_as_float(sr[e + h]) * cs - lse2);
-            if (need_mask) {
-              const int y_idx = y0 + c;
-              // key <= query when causal; padding rows past N see nothing.
-              const bool vis = y_idx < p.N &&
-                               (!p.causal || (kKV ? x_idx <= y_idx : y_idx <= x_idx));
-              if (!vis) pv = 0.0f;
+            for (int h = 0; h < 4; ++h) {
+              nl[h] = nlse_r;
+              nd[h] = nd_r;
             }
-            pe[h] = pv;
-            de[h] = pv * (__uint_as_float(dr[e + h]) - dd);
           }
-          pp[e / 2] = pack_bf16x2(pe[0], pe[1]);
-          pd[e / 2] = pack_bf16x2(de[0], de[1]);
+#pragma unroll
+          for (int h = 0; h < 4; h += 2) {
+            float x0, x1, p0, p1, t0, t1, d0, d1;
+            ffma2(x0, x1, __uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1]), cs, cs,
+                  nl[h], nl[h + 1]);
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+            if (need_mask) {
+              // key <= query when causal; padding rows past N see nothing.
+              const int ya = y0 + 32 * cc + e + h;
+              const bool va = ya < p.N && (!p.causal || (kKV ? x_idx <= ya : ya <= x_idx));
+              const bool vb = ya + 1 < p.N &&
+                              (!p.causal || (kKV ? x_idx <= ya + 1 : ya + 1 <= x_idx));
+              if (!va) p0 = 0.0f;
+              if (!vb) p1 = 0.0f;
+            }
+            fadd2(t0, t1, __uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1]), nd[h],
+                  nd[h + 1]);
+            fmul2(d0, d1, p0, p1, t0, t1);
+            pp[(e + h) / 2] = pack_bf16x2(p0, p1);
+            pd[(e + h) / 2] = pack_bf16x2(d0, d1);
+          }
         }
-        // Packed pairs of chunk cc land in columns [16cc, 16cc + 16), which
-        // this chunk has already read.
+        // Packed pairs of chunk cc land in columns [16cc, 16cc + 16) of the
+        // buffer, which this chunk has already read.
         if (kKV) {
-          tmem_st16(tmem + lane_off + C::kColS + 16 * cc, pp);
-          tmem_st16(tmem + lane_off + C::kColDP + 16 * cc, pd);
+          tmem_st16(tmem + lane_off + col_s + 16 * cc, pp);
+          tmem_st16(tmem + lane_off + col_dp + 16 * cc, pd);
         } else {
-          tmem_st16(tmem + lane_off + C::kColS + 16 * cc, pd);
+          tmem_st16(tmem + lane_off + col_s + 16 * cc, pd);
         }
       }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.p_full());
+      if (lane == 0) mbar_arrive(bars.p_full(g));
     }
     // ---------------------------------------------------------------- epilogue
+    // kKV: warpgroup 0 stores dK (scaled), warpgroup 1 dV; otherwise each
+    // warpgroup stores half of dQ's columns (scaled).
     if (ok && warp_wait_bar(bars.acc_done(), 0, wctx)) {
       tc_fence_after_sync();
       const bool in_range = x_idx < p.N;
+      constexpr int kCols = kKV ? D : D / 2;
+      const uint32_t col = kKV ? (g == 0 ? C::kColAcc0 : C::kColAcc1) : C::kColAcc0 + kCols * g;
+      const float mul = (kKV && g == 1) ? 1.0f : p.scale;
+      uint16_t* out = (kKV && g == 1) ? p.out1 : p.out0;
+      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * D +
+                                            (kKV ? 0 : kCols * g));
 #pragma unroll
-      for (int a = 0; a < (kKV ? 2 : 1); ++a) {
-        // kKV: a = 0 -> dK (scaled), a = 1 -> dV; otherwise dQ (scaled).
-        const uint32_t col = a == 0 ? C::kColAcc0 : C::kColAcc1;
-        const float mul = a == 0 ? p.scale : 1.0f;
-        uint16_t* out = a == 0 ? p.out0 : p.out1;
-        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * D);
+      for (int cc = 0; cc < kCols / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + col + 32 * cc, r);
+        tmem_ld_wait();
+        tmem_ld_fence(r);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + col + 32 * cc, r);
-          tmem_ld_wait();
-          tmem_ld_fence(r);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w4[4];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w4[e] = pack_bf16x2(__uint_as_float(r[8 * g + 2 * e]) * mul,
-                                  __uint_as_float(r[8 * g + 2 * e + 1]) * mul);
-            if (in_range) dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            w4[e] = pack_bf16x2(__uint_as_float(r[8 * q4 + 2 * e]) * mul,
+                                __uint_as_float(r[8 * q4 + 2 * e + 1]) * mul);
+          if (in_range) dst[4 * cc + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
     }
@@ -335,7 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     const bool leader = elect_one_sync();
     constexpr uint32_t kHi = desc_hi_sw128(1024);
-    constexpr uint32_t kIdescSS = idesc_bf16_f32(kBwdTile, kBwdTile, 0, 0);
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(kBwdTile, kBwdSub, 0, 0);
     constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBwdTile, D, 0, 1);
     const uint32_t x_lo = desc_lo(sX, 16);               // X tiles, K-major A
     const uint32_t yk_lo = desc_lo(sY, 16);              // Y tiles, K-major B
@@ -347,55 +379,84 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (leader) umma_commit(bar);
       __syncwarp();
     };
-    bool ok = warp_wait_bar(bars.x_full(), 0, wctx);
-    for (int n = 0; ok && n < steps; ++n) {
-      const int s = n % S;
-      if (!warp_wait_bar(bars.y_full(s), parity_of(n / S), wctx)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const uint32_t y0 = (s * C::kStageBytes) >> 4;
-      const uint32_t y1 = (s * C::kStageBytes + C::kTileBytes) >> 4;
+    // S and dP of sub-step m (buffer m & 1): X0 and X1 against the 64 rows
+    // 64 (m & 1) .. of the streamed tiles Y0 and Y1 (K-major, 8 KB in).
+    auto issue_sdp = [&](int m) {
+      const int b = m & 1;
+      const uint32_t st = ((m >> 1) % S) * C::kStageBytes + b * kBwdSub * 128;
+      const uint32_t y0 = yk_lo + (st >> 4);
+      const uint32_t y1 = yk_lo + ((st + C::kTileBytes) >> 4);
       constexpr uint32_t x1 = C::kTileBytes >> 4;
       if (leader) {
-        // S = X0 Y0^T and dP = X1 Y1^T over the head dimension.
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lohi(tmem + C::kColS, x_lo + kmaj_off(kk), kHi, yk_lo + y0 + kmaj_off(kk), kHi,
-                       kIdescSS, kk > 0 ? 1u : 0u);
+          umma_ss_lohi(tmem + C::kColS + kBwdSub * b, x_lo + kmaj_off(kk), kHi,
+                       y0 + kmaj_off(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lohi(tmem + C::kColDP, x_lo + x1 + kmaj_off(kk), kHi, yk_lo + y1 + kmaj_off(kk),
-                       kHi, kIdescSS, kk > 0 ? 1u : 0u);
+          umma_ss_lohi(tmem + C::kColDP + kBwdSub * b, x_lo + x1 + kmaj_off(kk), kHi,
+                       y1 + kmaj_off(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
       }
       __syncwarp();
-      commit(bars.st_full());
-      if (!warp_wait_bar(bars.p_full(), parity_of(n), wctx)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
+    };
+    // Accumulation of sub-step m over its 64 streamed rows, 16 per MMA; the
+    // A operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM buffer m & 1.
+    auto issue_acc = [&](int m) {
+      const int b = m & 1;
+      const uint32_t st = ((m >> 1) % S) * C::kStageBytes + b * kBwdSub * 128;
       if (leader) {
-        // Accumulate over the 128 rows of the Y tiles, 16 per MMA; the A
-        // operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM.
 #pragma unroll
-        for (int kk = 0; kk < kBwdTile / 16; ++kk) {
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t yoff = (kk * 16 * 128) >> 4;
+        for (int kk = 0; kk < kBwdSub / 16; ++kk) {
+          const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t r0 = (st + kk * 16 * 128) >> 4;
+          const uint32_t r1 = (st + C::kTileBytes + kk * 16 * 128) >> 4;
           if (kKV) {
-            umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + 8u * kk, ymn_lo + y1 + yoff, kHi,
-                         kIdescAcc, acc);  // dV += P^T dO
-            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColDP + 8u * kk, ymn_lo + y0 + yoff, kHi,
-                         kIdescAcc, acc);  // dK += dS^T Q
+            umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + kBwdSub * b + 8u * kk,
+                         ymn_lo + r1, kHi, kIdescAcc, acc);  // dV += P^T dO
+            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColDP + kBwdSub * b + 8u * kk,
+                         ymn_lo + r0, kHi, kIdescAcc, acc);  // dK += dS^T Q
           } else {
-            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColS + 8u * kk, ymn_lo + y0 + yoff, kHi,
-                         kIdescAcc, acc);  // dQ += dS K
+            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColS + kBwdSub * b + 8u * kk,
+                         ymn_lo + r0, kHi, kIdescAcc, acc);  // dQ += dS K
           }
         }
       }
       __syncwarp();
-      commit(bars.y_empty(s));
+    };
+    const int M = 2 * steps;
+    bool ok = warp_wait_bar(bars.x_full(), 0, wctx) &&
+              warp_wait_bar(bars.y_full(0), 0, wctx);
+    if (ok) {
+      tc_fence_after_sync();
+      issue_sdp(0);
+      commit(bars.st_full(0));
+      issue_sdp(1);
+      commit(bars.st_full(1));
+    }
+    for (int m = 0; ok && m < M; ++m) {
+      const int b = m & 1;
+      if (!warp_wait_bar(bars.p_full(b), parity_of(m >> 1), wctx)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      issue_acc(m);
+      if (b == 1) commit(bars.y_empty((m >> 1) % S));  // both halves of the tile consumed
+      const int m2 = m + 2;
+      if (m2 < M) {
+        // S, dP of sub-step m + 2 overwrite buffer b after the accumulation
+        // that reads it (MMAs of one thread run in issue order).
+        if ((m2 & 1) == 0) {
+          const int n2 = m2 >> 1;
+          if (!warp_wait_bar(bars.y_full(n2 % S), parity_of(n2 / S), wctx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        issue_sdp(m2);
+        commit(bars.st_full(b));
+      }
     }
     // Every MMA issued has completed once acc_done fires.
     commit(bars.acc_done());
