@@ -163,6 +163,20 @@ def dist_setup():
     return world, rank, local
 
 
+def order1_bytes(w) -> float:
+    """Algorithmic HBM bytes of the K/V-outer loop order (64 x 64 tiles):
+    K and V read once; per visible (query tile, key tile) step Q_i read and
+    the running fp32 O_i, m_i, l_i read (after the first step) and written
+    (before the last); O (bf16) and LSE written once."""
+    t = -(-w.N // 64)
+    steps = t * (t + 1) // 2 if w.causal else t * t
+    per_tile_q = 64 * w.d * 2
+    state = 64 * (w.d + 2) * 4
+    bh = w.B * w.H
+    return bh * (2 * w.N * w.d * 2 + steps * per_tile_q + 2 * (steps - t) * state
+                 + w.N * w.d * 2 + w.N * 4)
+
+
 def cpu_oracle_sample_decode(w, qkv, heads: int, threads: int = 0, min_seconds: float = 0.0):
     """Time the fp64 oracle on the first `heads` (batch, head) slices of a
     decode workload, repeated until `min_seconds` have passed (at least
@@ -298,6 +312,13 @@ def run_ours(args, w):
 
         def step():
             fa.fa_fwd_splitkv(qd, kd, vd, o, lse, w.causal, w.scale, 0, workspace, stream)
+    elif args.loop_order:
+        ws_ord = torch.empty(max(16, fa.load_library().fa_fwd_order_ablation_workspace_bytes(
+            w.B, w.H, w.N, w.d, args.loop_order)), dtype=torch.uint8, device=dev)
+
+        def step():
+            fa.attention_forward_order_ablation(qd, kd, vd, w.causal, w.scale, args.loop_order,
+                                                workspace=ws_ord, out=(o, lse), stream=stream)
     else:
         def step():
             fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
@@ -418,6 +439,21 @@ def run_ours(args, w):
                    "sample": (f"{n_rows} seeded query rows per head x {w.B * w.H} heads "
                               f"({100.0 * n_rows / w.N:.2f}% of the rows), fp64 oracle, "
                               f"{dt:.1f} s")}
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
+                        "; fp16 x 1: its nominal dense rate equals bf16's"
+                        if elem == "f16" else ""),
+                    "traffic": None if args.loop_order else NCU_TRAFFIC_BYTES.get(w.name)}
+        if args.loop_order == 1:
+            # The K/V-outer order moves the running state through HBM every
+            # step: its own algorithmic bytes bound it.
+            nbytes = order1_bytes(w)
+            roofline = {"bound": "hbm", "achieved": nbytes / avg_launch_s / 1e9,
+                        "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                        "frac": nbytes / avg_launch_s / 1e9 / float(peaks["hbm_gbs"]),
+                        "peak_source": f"{peaks_src} hbm_gbs",
+                        "algorithmic_bytes": nbytes, "traffic": None}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -426,14 +462,12 @@ def run_ours(args, w):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "causal": w.causal, "scale": w.scale,
                        "l2": "flushed between launches (256 MiB write, untimed)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       **({"loop_order": {1: "K/V outer (v1)", 2: "Q outer (v2)"}[args.loop_order],
+                           "kernel": "fa_fwd_order_ablation (64x64 tiles, warp MMAs)"}
+                          if args.loop_order else {})},
             "pct_of_peak": 100.0 * achieved / peak,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
-                             "; fp16 x 1: its nominal dense rate equals bf16's"
-                             if elem == "f16" else ""),
-                         "traffic": NCU_TRAFFIC_BYTES.get(w.name)},
+            "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -629,6 +663,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="query rows per head per step of --impl reference")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--loop-order", type=int, choices=(1, 2), default=0,
+                    help="time the loop-order ablation kernel instead of fa_fwd: 1 = K/V "
+                         "outer (v1), 2 = Q outer (v2)")
     ap.add_argument("--pass", dest="pass_", choices=("fwd", "bwd"), default="fwd",
                     help="bwd: time the backward pass of the (square) workload")
     args = ap.parse_args(argv)

@@ -212,6 +212,35 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 /* Workspace bytes fa_bwd needs (0 on invalid arguments). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
+/*
+ * fa_fwd_order_ablation — the attention forward of fa_fwd in one of the two
+ * loop orders the pages compare, for measuring their HBM traffic and time
+ * side by side (a measurement instrument; fa_fwd is the production path).
+ *
+ *   order 1: "Parsing FlashAttention (2): FlashAttention-v1 forward pass" §4
+ *            Algorithm 1 — per (batch, head), K/V tiles outer and query tiles
+ *            inner; every step reads Q_i and the running O_i, m_i, l_i from
+ *            the workspace in HBM and writes them back (normalised update,
+ *            eq. (37)); one CTA per (batch, head).
+ *   order 2: "Online Softmax and FlashAttention" (course unit 12) — query
+ *            tiles outer with Q_i and the accumulator on chip, K/V tiles
+ *            streamed, O written once; one CTA per (batch, head, query tile).
+ * Both run the same 64 x 64 tile code on warp-level tensor-core MMAs.
+ *
+ *   q, k, v, o, lse, B, H, N, causal, scale : as for fa_fwd (contiguous bf16)
+ *   d          : 64 or 128
+ *   workspace  : at least fa_fwd_order_ablation_workspace_bytes() bytes of
+ *                device memory (16-byte aligned), owned by the caller,
+ *                overwritten (order 1: the running fp32 O, m, l of every row)
+ * Returns FA_OK or an FA_ERR_* code; validates before enqueueing; async.
+ */
+int fa_fwd_order_ablation(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int H, int N, int d, int causal, float scale, int order,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of fa_fwd_order_ablation (0 on invalid arguments). */
+size_t fa_fwd_order_ablation_workspace_bytes(int B, int H, int N, int d, int order);
+
 /* Human-readable text for a return code (static storage, never NULL). */
 const char *fa_strerror(int code);
 

@@ -20,7 +20,7 @@ __all__ = [
     "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version", "fa_fwd_strided",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
-    "fa_bwd", "fa_bwd_workspace_bytes", "attention_backward",
+    "fa_bwd", "fa_bwd_workspace_bytes", "attention_backward", "attention_forward_order_ablation",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
     "fa_set_fault_injection", "load_library", "LIB_PATH",
     "FA_DEVICE_STATUS_TIMEOUT", "FA_INJECT_SKIP_FIRST_V_LOAD",
@@ -85,6 +85,11 @@ def load_library(path: str | None = None):
                                ctypes.c_size_t, vp]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_fwd_order_ablation.restype = i
+        lib.fa_fwd_order_ablation.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                              ctypes.c_size_t, vp]
+        lib.fa_fwd_order_ablation_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_order_ablation_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.fa_fwd_splitkv_static.restype = i
         lib.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_splitkv_static_scratch_bytes.restype = ctypes.c_size_t
@@ -358,6 +363,38 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, None, stream)
     return dq, dk, dv
+
+
+def attention_forward_order_ablation(q, k, v, causal: bool, scale: float, order: int,
+                                     workspace=None, out=None, stream=None):
+    """The forward in loop order 1 (K/V outer, O/m/l through HBM) or 2 (Q
+    outer, state on chip) via ``fa_fwd_order_ablation``; contiguous bf16
+    ``[B, H, N, d]`` CUDA tensors, d 64 or 128.  Returns ``(O, LSE)``
+    (``out`` = preallocated ``(O, LSE)`` to reuse)."""
+    import torch
+
+    B, H, N, d = _dims(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or \
+                tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, H, N, d]")
+    with torch.cuda.device(q.device):
+        if out is None:
+            out = (torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32,
+                                                    device=q.device))
+        o, lse = out
+        if workspace is None:
+            nbytes = load_library().fa_fwd_order_ablation_workspace_bytes(B, H, N, d, order)
+            workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        rc = load_library().fa_fwd_order_ablation(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+            int(bool(causal)), float(scale), int(order), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), handle or None)
+        _check(rc, "fa_fwd_order_ablation")
+    return o, lse
 
 
 def fa_get_device_status() -> int:

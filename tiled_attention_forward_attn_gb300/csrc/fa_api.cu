@@ -13,6 +13,7 @@
 #include "fa.h"
 #include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
+#include "fa_order_ablation.cuh"
 #include "fa_splitkv.cuh"
 
 namespace {
@@ -74,6 +75,12 @@ cudaError_t configure_bwd_kernel() {
                               static_cast<int>(fa::BwdCfg<D, kKV>::kSmemAlloc));
 }
 
+template <int D, bool kV1>
+cudaError_t configure_order_kernel() {
+  return cudaFuncSetAttribute(fa::fa_order_kernel<D, kV1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::OrdCfg<D, kV1>::kSmemAlloc));
+}
+
 template <int D>
 cudaError_t configure_split_kernel() {
   return cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D>,
@@ -109,7 +116,11 @@ int prepare_device(int* dev_out, int* sms_out) {
       configure_bwd_kernel<64, true>() != cudaSuccess ||
       configure_bwd_kernel<64, false>() != cudaSuccess ||
       configure_bwd_kernel<128, true>() != cudaSuccess ||
-      configure_bwd_kernel<128, false>() != cudaSuccess)
+      configure_bwd_kernel<128, false>() != cudaSuccess ||
+      configure_order_kernel<64, true>() != cudaSuccess ||
+      configure_order_kernel<64, false>() != cudaSuccess ||
+      configure_order_kernel<128, true>() != cudaSuccess ||
+      configure_order_kernel<128, false>() != cudaSuccess)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
   *sms_out = sms;
@@ -417,6 +428,90 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return d == 64 ? launch_bwd<64>(o, dout, lse, mq, mk, mv, mdo, prm, prm_q, st)
                  : launch_bwd<128>(o, dout, lse, mq, mk, mv, mdo, prm, prm_q, st);
+}
+
+// ------------------------------------------------------- loop-order ablation
+
+namespace {
+
+int64_t ord_npad(int N) { return (static_cast<int64_t>(N) + fa::kOrdTile - 1) / fa::kOrdTile * fa::kOrdTile; }
+
+template <int D>
+int launch_order(int order, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                 const fa::OrderParams& prm, cudaStream_t stream) {
+  if (order == 1) {
+    fa::fa_order_kernel<D, true><<<static_cast<unsigned>(prm.num_bh), fa::kOrdThreads,
+                                   fa::OrdCfg<D, true>::kSmemAlloc, stream>>>(mq, mk, mv, prm);
+  } else {
+    const unsigned ctas = static_cast<unsigned>(static_cast<int64_t>(prm.T) * prm.num_bh);
+    fa::fa_order_kernel<D, false><<<ctas, fa::kOrdThreads, fa::OrdCfg<D, false>::kSmemAlloc,
+                                    stream>>>(mq, mk, mv, prm);
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" size_t fa_fwd_order_ablation_workspace_bytes(int B, int H, int N, int d, int order) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || (order != 1 && order != 2)) return 0;
+  if (order == 2) return 16;  // the v2 order keeps its state on chip
+  const int64_t rows = static_cast<int64_t>(B) * H * ord_npad(N);
+  return static_cast<size_t>(rows * (static_cast<int64_t>(d) + 2) * 4);
+}
+
+extern "C" int fa_fwd_order_ablation(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     int B, int H, int N, int d, int causal, float scale, int order,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1) || (order != 1 && order != 2))
+    return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t Npad = ord_npad(N);
+  if (BH > 65535 || BH * Npad > INT_MAX / 4) return FA_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+       reinterpret_cast<uintptr_t>(workspace)) &
+      15u)
+    return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  const size_t need = fa_fwd_order_ablation_workspace_bytes(B, H, N, d, order);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const size_t tb = static_cast<size_t>(BH) * N * d * 2, lb = static_cast<size_t>(BH) * N * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb) || overlaps(workspace, need, in, tb))
+      return FA_ERR_ALIAS;
+  if (overlaps(o, tb, lse, lb) || overlaps(workspace, need, o, tb) || overlaps(workspace, need, lse, lb))
+    return FA_ERR_ALIAS;
+
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
+  if (prep != FA_OK) return prep;
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return FA_ERR_LAUNCH;
+  CUtensorMap mq, mk, mv;
+  if (!encode_map(&mq, q, static_cast<int>(BH), N, d, fa::kOrdTile) ||
+      !encode_map(&mk, k, static_cast<int>(BH), N, d, fa::kOrdTile) ||
+      !encode_map(&mv, v, static_cast<int>(BH), N, d, fa::kOrdTile))
+    return FA_ERR_LAUNCH;
+  fa::OrderParams prm;
+  prm.o = static_cast<uint16_t*>(o);
+  prm.lse = lse;
+  float* ws = static_cast<float*>(workspace);
+  prm.ws_o = ws;
+  prm.ws_m = ws + BH * Npad * d;
+  prm.ws_l = prm.ws_m + BH * Npad;
+  prm.N = N;
+  prm.Npad = static_cast<int>(Npad);
+  prm.T = static_cast<int>(Npad / fa::kOrdTile);
+  prm.num_bh = static_cast<int>(BH);
+  prm.causal = causal;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_order<64>(order, mq, mk, mv, prm, st)
+                 : launch_order<128>(order, mq, mk, mv, prm, st);
 }
 
 // ---------------------------------------------------------------- split-KV
