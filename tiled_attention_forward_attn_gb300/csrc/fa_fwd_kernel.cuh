@@ -123,9 +123,9 @@ struct Cfg {
   static constexpr uint32_t kOffK = kOffQ + kTilesPerCta * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStagesK * kKVBytes;
   static constexpr uint32_t kOffBar = kOffV + kStagesV * kKVBytes;
-  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done,
+  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, p_half[2],
   // k_full[SK], k_empty[SK], v_full[SV], v_empty[SV]
-  static constexpr int kNumBars = 11 + 2 * kStagesK + 2 * kStagesV;
+  static constexpr int kNumBars = 13 + 2 * kStagesK + 2 * kStagesV;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -145,10 +145,11 @@ struct Barriers {
   __device__ uint32_t p_full(int t) const { return base + 48u + 8u * t; }
   __device__ uint32_t o_done(int t) const { return base + 64u + 8u * t; }
   __device__ uint32_t mma_done() const { return base + 80u; }
-  __device__ uint32_t k_full(int s) const { return base + 88u + 8u * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 88u + 8u * (sk + s); }
-  __device__ uint32_t v_full(int s) const { return base + 88u + 8u * (2 * sk + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 88u + 8u * (2 * sk + sv + s); }
+  __device__ uint32_t p_half(int t) const { return base + 88u + 8u * t; }
+  __device__ uint32_t k_full(int s) const { return base + 104u + 8u * s; }
+  __device__ uint32_t k_empty(int s) const { return base + 104u + 8u * (sk + s); }
+  __device__ uint32_t v_full(int s) const { return base + 104u + 8u * (2 * sk + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 104u + 8u * (2 * sk + sv + s); }
 };
 
 struct WaitCtx {
@@ -328,7 +329,10 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
 
     // P = 2^(s*c - m_ref) and its row sum; P_t goes, as 16-bit pairs, over the
     // first 64 columns of S_t (whose values are already in registers), in
-    // two halves so that half of the scores are dead before the second.
+    // two halves of 64 keys so that half of the scores are dead before the
+    // second.  Each half is handed over on its own (p_half, then p_full):
+    // the P.V MMAs of the first 64 keys start while the second half of P is
+    // still being computed.
     const float neg_m = -m_ref;
     float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
 #pragma unroll
@@ -348,33 +352,32 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
         pk[i / 2 + 1] = pack_x2<kF16>(p2, p3);
       }
       tmem_st32(s_addr + 32 * h, pk);
+      if (h == 0 && rescale && j > 0) {
+        // O_t holds every P.V product up to tile j-1 (the S_t(j) MMA was
+        // committed after them) and no MMA touches it until p_half: rescale
+        // it in place, before the first half of P is handed over.
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + 32 * cc, o);
+          tmem_ld_wait();
+          tmem_ld_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float a0, a1;
+            fmul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+            o[i] = __float_as_uint(a0);
+            o[i + 1] = __float_as_uint(a1);
+          }
+          tmem_st32(o_addr + 32 * cc, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(h == 0 ? bars.p_half(t) : bars.p_full(t));
     }
     l_run += (sa0 + sa1) + (sb0 + sb1);
-
-    if (rescale && j > 0) {
-      // O_t holds every P.V product up to tile j-1 (the S_t(j) MMA was
-      // committed after them) and no MMA touches it until p_full: rescale
-      // it in place.
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + 32 * cc, o);
-        tmem_ld_wait();
-        tmem_ld_fence(o);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float a0, a1;
-          fmul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-          o[i] = __float_as_uint(a0);
-          o[i + 1] = __float_as_uint(a1);
-        }
-        tmem_st32(o_addr + 32 * cc, o);
-      }
-    }
-    tmem_st_wait();
-    tc_fence_before_sync();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bars.p_full(t));
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -439,6 +442,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.q_empty(t), 1);
       mbar_init(bars.s_full(t), 1);
       mbar_init(bars.p_full(t), kRowThreadsPerTile / 32);  // one arrival per warp
+      mbar_init(bars.p_half(t), kRowThreadsPerTile / 32);
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.mma_done(), 1);
@@ -632,16 +636,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int t, uint32_t v_stage, bool first) {  // O_t (+)= P_t V
+    // O_t (+)= P_t V over keys 64h .. 64h + 63 (V slices 4h .. 4h + 3).
+    auto issue_pv = [&](int t, uint32_t v_stage, bool first, int h) {
       const uint32_t b_lo = v_lo + ((v_stage * C::kKVBytes) >> 4);
       const uint32_t p_tmem = tmem + C::kColS + 128u * t;
       const uint32_t d_tmem = tmem + C::kColO + static_cast<uint32_t>(D) * t;
-      const uint32_t acc0 = first ? 0u : 1u;
+      const uint32_t acc0 = (first && h == 0) ? 0u : 1u;
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)  // V slice kk: 16 key rows of 128 bytes
+        for (int k4 = 0; k4 < kBlockN / 32; ++k4) {  // V slice kk: 16 key rows of 128 bytes
+          const int kk = (kBlockN / 32) * h + k4;
           umma_ts_lohi(d_tmem, p_tmem + 8u * kk, b_lo + ((kk * 16 * 128) >> 4), kHi, idesc_pv,
-                       kk > 0 ? 1u : acc0);
+                       k4 > 0 ? 1u : acc0);
+        }
       }
       __syncwarp();
     };
@@ -686,13 +693,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int t = 0; t < kTilesPerCta; ++t) {
           const int n = t == 0 ? u.n[0] : u.n[1];
           if (!ok || j >= n) continue;
+          if (!warp_wait_bar(bars.p_half(t), parity_of(pc[t]), wctx)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after_sync();
+          issue_pv(t, vc % SV, j == 0, 0);
           if (!warp_wait_bar(bars.p_full(t), parity_of(pc[t]), wctx)) {
             ok = false;
             continue;
           }
           ++pc[t];
           tc_fence_after_sync();
-          issue_pv(t, vc % SV, j == 0);
+          issue_pv(t, vc % SV, j == 0, 1);
           // V_j is free once the last tile that reads it has its P.V issued
           // (released before the S MMA that follows, to refill the ring early).
           if (t == kTilesPerCta - 1 || j >= u.n[kTilesPerCta - 1]) commit(bars.v_empty(vc % SV));
