@@ -65,7 +65,7 @@ enum fa_status {
  *   lse     : fp32 [B][H][N], contiguous (device), written; natural-log units
  *             of the scaled, masked scores: LSE_i = ln sum_j exp(S_ij)
  *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1
- *   d       : head dimension, a multiple of 16 from 16 to 128
+ *   d       : head dimension, a multiple of 16 from 16 to 128, or 256
  *   causal  : 0 = full attention, 1 = query i sees keys 0..i (square,
  *             top-left aligned)
  *   scale   : any finite float multiplying Q K^T (typically 1/sqrt(d))

@@ -74,12 +74,12 @@ def test_bad_shapes_rejected(lib, kw):
     assert _call(lib, **kw) == FA_ERR_SHAPE
 
 
-@pytest.mark.parametrize("d", [0, 8, 24, 127, 144, 256])
+@pytest.mark.parametrize("d", [0, 8, 24, 127, 144, 192, 240, 272])
 def test_unsupported_head_dim_rejected(lib, d):
     assert _call(lib, d=d) == FA_ERR_HEAD_DIM
 
 
-@pytest.mark.parametrize("d", [16, 32, 48, 80, 96, 112])
+@pytest.mark.parametrize("d", [16, 32, 48, 80, 96, 112, 256])
 def test_multiple_of_16_head_dims_accepted(lib, d):
     import torch
 

@@ -74,6 +74,47 @@ def test_head_dim_outputs_stay_in_bounds(fa, cuda_device):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 65, 129, 300, 1000])
+def test_head_dim_256_matches_oracle(fa, cuda_device, N, causal, dtype):
+    q, k, v = workloads.generate_shape(2, 2, N, 256, seed=680 + N, qk_std=1.5, dtype=dtype)
+    scale = 1.0 / 16.0
+    o, lse = _run(fa, cuda_device, q, k, v, causal, scale, dtype)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, scale, dtype=dtype)
+    compare(o, lse, o_ref, lse_ref, label=f"d256 N{N} c{causal} {dtype}")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.15])
+def test_head_dim_256_unusual_scales(fa, cuda_device, scale):
+    q, k, v = workloads.generate_shape(1, 2, 400, 256, seed=690)
+    o, lse = _run(fa, cuda_device, q, k, v, True, scale, "bf16")
+    o_ref, lse_ref = oracle.attention(q, k, v, True, scale)
+    compare(o, lse, o_ref, lse_ref, label=f"d256 scale {scale}")
+
+
+def test_head_dim_256_strided(fa, cuda_device):
+    """[B, N, H, d] memory with d = 256, causal, more units than SMs."""
+    import torch
+
+    B, H, N, d = 2, 8, 1500, 256
+    q, k, v = workloads.generate_shape(B, H, N, d, seed=695, qk_std=1.5)
+
+    def bnhd(a):
+        return workloads.as_torch(a).permute(0, 2, 1, 3).contiguous().to(cuda_device).permute(
+            0, 2, 1, 3)
+
+    qd, kd, vd = bnhd(q), bnhd(k), bnhd(v)
+    o = torch.empty((B, N, H, d), dtype=qd.dtype, device=cuda_device).permute(0, 2, 1, 3)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=cuda_device)
+    fa.fa_fwd(qd, kd, vd, o, lse, True, 0.0625)
+    torch.cuda.synchronize(cuda_device)
+    rows = np.unique(np.concatenate([np.arange(0, N, 7), [N - 1]]))
+    o_ref, lse_ref = oracle.attention(q, k, v, True, 0.0625, rows=rows)
+    compare(o.float().cpu().numpy()[:, :, rows], lse.cpu().numpy()[:, :, rows], o_ref, lse_ref,
+            label="d256 bnhd")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_strided_bnhd_layout(fa, cuda_device, dtype):
     """Q, K, V and O in [B, N, H, d] memory (heads interleaved within a row),
     viewed as [B, H, N, d]."""

@@ -14,8 +14,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
 SOURCES = ("fa_api.cu",)
-HEADERS = ("fa_bwd_kernel.cuh", "fa_fwd_kernel.cuh", "fa_order_ablation.cuh", "fa_splitkv.cuh",
-           "ptx.cuh")
+HEADERS = ("fa_bwd_kernel.cuh", "fa_fwd_d256.cuh", "fa_fwd_kernel.cuh", "fa_order_ablation.cuh",
+           "fa_splitkv.cuh", "ptx.cuh")
 
 NVCC_FLAGS = (
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_bwd_kernel.cuh"
+#include "fa_fwd_d256.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_order_ablation.cuh"
 #include "fa_splitkv.cuh"
@@ -63,6 +64,13 @@ bool configure_both_signs() {
          configure_kernel<D, true, kF16, kPartialD>() == cudaSuccess;
 }
 
+template <bool kNeg, bool kF16>
+cudaError_t configure_d256() {
+  return cudaFuncSetAttribute(fa::fa_fwd_d256_kernel<kNeg, kF16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::WideCfg::kSmemAlloc));
+}
+
 template <int D>
 bool configure_dim() {
   return configure_both_signs<D, false, false>() && configure_both_signs<D, true, false>() &&
@@ -112,6 +120,8 @@ int prepare_device(int* dev_out, int* sms_out) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
   if (!configure_dim<64>() || !configure_dim<128>() ||
+      configure_d256<false, false>() != cudaSuccess || configure_d256<true, false>() != cudaSuccess ||
+      configure_d256<false, true>() != cudaSuccess || configure_d256<true, true>() != cudaSuccess ||
       configure_split_kernel<64>() != cudaSuccess || configure_split_kernel<128>() != cudaSuccess ||
       configure_bwd_kernel<64, true>() != cudaSuccess ||
       configure_bwd_kernel<64, false>() != cudaSuccess ||
@@ -160,6 +170,19 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+template <bool kF16>
+int launch_d256(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                const fa::FwdParams& prm, int sms, cudaStream_t stream) {
+  const unsigned ctas = static_cast<unsigned>(prm.total_units < sms ? prm.total_units : sms);
+  if (prm.scale_log2 < 0.0f)
+    fa::fa_fwd_d256_kernel<true, kF16><<<ctas, fa::kW_Threads, fa::WideCfg::kSmemAlloc, stream>>>(
+        mq, mk, mv, prm);
+  else
+    fa::fa_fwd_d256_kernel<false, kF16><<<ctas, fa::kW_Threads, fa::WideCfg::kSmemAlloc, stream>>>(
+        mq, mk, mv, prm);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 template <int D, bool kF16, bool kPartialD>
 int launch_sign(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                 const fa::FwdParams& prm, int sms, cudaStream_t stream) {
@@ -171,7 +194,7 @@ int launch_sign(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
 // as a 4-D tensor map {d, N, H, B}: boxes of 64 columns x 128 rows x 1 x 1
 // with the 128-byte swizzle; columns past d and rows past N read as zero.
 bool encode_map4(CUtensorMap* map, const void* ptr, CUtensorMapDataType type, int B, int H, int N,
-                 int d, const int64_t* st) {
+                 int d, const int64_t* st, int box_rows = 128) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   // A dimension of extent 1 is never stepped; give it a harmless stride.
@@ -180,7 +203,7 @@ bool encode_map4(CUtensorMap* map, const void* ptr, CUtensorMapDataType type, in
     return static_cast<cuuint64_t>(extent == 1 && bytes == 0 ? 16 : bytes);
   };
   const cuuint64_t strides[3] = {stride(2, N), stride(1, H), stride(0, B)};
-  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
   const CUresult r =
       g_encode(map, type, 4, const_cast<void*>(ptr), dims, strides, box, elem_strides,
@@ -226,10 +249,12 @@ int fwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* 
              int dtype, int B, int H, int N, int d, int causal, float scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_SHAPE;
-  if (d < 16 || d > 128 || d % 16 != 0) return FA_ERR_HEAD_DIM;
+  if (d != 256 && (d < 16 || d > 128 || d % 16 != 0)) return FA_ERR_HEAD_DIM;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t num_units = (static_cast<int64_t>(N) + fa::kUnitM - 1) / fa::kUnitM;
+  // Work units: 256-row query units, or single 128-row query tiles at d = 256.
+  const int64_t unit_rows = d == 256 ? fa::kW_TileM : fa::kUnitM;
+  const int64_t num_units = (static_cast<int64_t>(N) + unit_rows - 1) / unit_rows;
   // Work units (B*H x 256-row query units) are counted in int, and so are
   // the row offsets bh*N + row of the LSE store.
   if (BH > INT_MAX || BH * num_units > INT_MAX || BH * N > INT_MAX) return FA_ERR_SHAPE;
@@ -267,9 +292,12 @@ int fwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* 
 
   const CUtensorMapDataType tt =
       dtype == FA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // d = 256 streams 64-key K/V tiles; otherwise 128-key tiles.
+  const int kv_rows = d == 256 ? fa::kW_BlockN : 128;
   CUtensorMap mq, mk, mv;
-  if (!encode_map4(&mq, q, tt, B, H, N, d, qs) || !encode_map4(&mk, k, tt, B, H, N, d, ks) ||
-      !encode_map4(&mv, v, tt, B, H, N, d, vs))
+  if (!encode_map4(&mq, q, tt, B, H, N, d, qs) ||
+      !encode_map4(&mk, k, tt, B, H, N, d, ks, kv_rows) ||
+      !encode_map4(&mv, v, tt, B, H, N, d, vs, kv_rows))
     return FA_ERR_LAUNCH;
 
   const bool f16 = dtype == FA_DTYPE_FP16;
@@ -299,6 +327,8 @@ int fwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* 
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 256)
+    return f16 ? launch_d256<true>(mq, mk, mv, prm, sms, st) : launch_d256<false>(mq, mk, mv, prm, sms, st);
   if (d == 128)
     return f16 ? launch_sign<128, true, false>(mq, mk, mv, prm, sms, st)
                : launch_sign<128, false, false>(mq, mk, mv, prm, sms, st);
@@ -762,7 +792,8 @@ extern "C" const char* fa_strerror(int code) {
     case FA_ERR_NULL: return "a required pointer is NULL";
     case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and within index limits; causal 0 or 1)";
     case FA_ERR_HEAD_DIM:
-      return "unsupported head dimension (fa_fwd: a multiple of 16 in 16..128; split-KV: 64 or 128)";
+      return "unsupported head dimension (fa_fwd: a multiple of 16 in 16..128, or 256; split-KV "
+             "and backward: 64 or 128)";
     case FA_ERR_ALIGN: return "misaligned pointer (q, k, v, o need 16 bytes; lse needs 4)";
     case FA_ERR_SCALE: return "scale is not finite";
     case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
