@@ -77,8 +77,14 @@ bool configure_dim() {
          configure_both_signs<D, false, true>() && configure_both_signs<D, true, true>();
 }
 
+// As for the forward: the register split (setmaxnreg) assumes the launch
+// register count.
 template <int D, bool kKV>
 cudaError_t configure_bwd_kernel() {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_bwd_kernel<D, kKV>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != static_cast<int>(fa::kBwdLaunchRegs)) return cudaErrorInvalidKernelImage;
   return cudaFuncSetAttribute(fa::fa_bwd_kernel<D, kKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::BwdCfg<D, kKV>::kSmemAlloc));
 }
@@ -366,10 +372,13 @@ int64_t bwd_npad(int N) { return (static_cast<int64_t>(N) + fa::kBwdTile - 1) / 
 
 // Three launches on one stream: D and LSE*log2(e) into the workspace, the
 // dK/dV pass (prm_kv: out0 = dK, out1 = dV), the dQ pass (prm_q: out0 = dQ).
+// mX: 128-row boxes (stationary tiles); mX64: 64-row boxes (streamed halves).
 template <int D>
 int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensorMap& mq,
                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-               const fa::BwdParams& base, const fa::BwdParams& prm_q, cudaStream_t stream) {
+               const CUtensorMap& mq64, const CUtensorMap& mk64, const CUtensorMap& mv64,
+               const CUtensorMap& mdo64, const fa::BwdParams& base, const fa::BwdParams& prm_q,
+               cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(base.num_bh) * base.Npad;
   const int64_t threads = rows * (D / 8);  // a multiple of 256: Npad is a multiple of 128
   fa::fa_bwd_prep_kernel<D><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
@@ -378,10 +387,10 @@ int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensor
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   const unsigned ctas = static_cast<unsigned>(static_cast<int64_t>(base.T) * base.num_bh);
   fa::fa_bwd_kernel<D, true><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, true>::kSmemAlloc, stream>>>(
-      mk, mv, mq, mdo, base);
+      mk, mv, mq64, mdo64, base);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa::fa_bwd_kernel<D, false><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, false>::kSmemAlloc, stream>>>(
-      mq, mdo, mk, mv, prm_q);
+      mq, mdo, mk64, mv64, prm_q);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -431,11 +440,13 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if (prep != FA_OK) return prep;
   std::call_once(g_encode_once, load_encode);
   if (g_encode == nullptr) return FA_ERR_LAUNCH;
-  CUtensorMap mq, mk, mv, mdo;
-  if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
-      !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
-      !encode_map(&mv, v, static_cast<int>(BH), N, d) ||
-      !encode_map(&mdo, dout, static_cast<int>(BH), N, d))
+  CUtensorMap mq, mk, mv, mdo, mq64, mk64, mv64, mdo64;
+  const int bhi = static_cast<int>(BH);
+  if (!encode_map(&mq, q, bhi, N, d) || !encode_map(&mk, k, bhi, N, d) ||
+      !encode_map(&mv, v, bhi, N, d) || !encode_map(&mdo, dout, bhi, N, d) ||
+      !encode_map(&mq64, q, bhi, N, d, fa::kBwdSub) || !encode_map(&mk64, k, bhi, N, d, fa::kBwdSub) ||
+      !encode_map(&mv64, v, bhi, N, d, fa::kBwdSub) ||
+      !encode_map(&mdo64, dout, bhi, N, d, fa::kBwdSub))
     return FA_ERR_LAUNCH;
 
   fa::BwdParams prm;
@@ -456,8 +467,10 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   prm_q.out0 = static_cast<uint16_t*>(dq);
   prm_q.out1 = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_bwd<64>(o, dout, lse, mq, mk, mv, mdo, prm, prm_q, st)
-                 : launch_bwd<128>(o, dout, lse, mq, mk, mv, mdo, prm, prm_q, st);
+  return d == 64 ? launch_bwd<64>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
+                                  prm_q, st)
+                 : launch_bwd<128>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
+                                   prm_q, st);
 }
 
 // ------------------------------------------------------- loop-order ablation

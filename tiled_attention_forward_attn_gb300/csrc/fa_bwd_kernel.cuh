@@ -36,8 +36,8 @@
 // buffers [0,64) and [64,128), dP buffers [128,192) and [192,256), then the
 // accumulators (dK and dV, or dQ), D columns each.  Warps: 0-3 and 4-7
 // elementwise (buffer 0 and 1) and epilogue, 8 the TMA producer, 9 the TMEM
-// allocator and MMA issuer.  Every wait is bounded like the forward's
-// (status word, drain, TMEM freed).
+// allocator and MMA issuer, 10-11 idle.  Every wait is bounded like the
+// forward's (status word, drain, TMEM freed).
 #pragma once
 
 #include <cstdint>
@@ -49,9 +49,18 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 320;
+// Three warpgroups: two elementwise, one with the producer, the MMA issuer
+// and two idle warps.  Launched with 168 registers a thread (65536 / 384,
+// rounded to what three warps per sub-partition allow); setmaxnreg then
+// moves registers from the control warpgroup to the elementwise ones.
+constexpr int kBwdThreads = 384;
 constexpr int kBwdLoadWarp = 8;
 constexpr int kBwdMmaWarp = 9;
+constexpr uint32_t kBwdLaunchRegs = 168;
+constexpr uint32_t kBwdEwRegs = 200;
+constexpr uint32_t kBwdControlRegs = 104;
+static_assert(2 * 128 * kBwdEwRegs + 128 * kBwdControlRegs <= kBwdThreads * kBwdLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kBwdTile = 128;  // rows of every tile (keys or queries)
 constexpr int kBwdSub = 64;    // streamed rows per sub-step
 
@@ -73,14 +82,19 @@ struct BwdParams {
 template <int D, bool kKV>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dimension");
-  static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr uint32_t kTileBytes = kBwdTile * D * 2;
-  static constexpr uint32_t kVecBytes = kKV ? 1024 : 0;  // -LSE2[128] then -D[128], fp32
-  static constexpr uint32_t kStageBytes = 2 * kTileBytes + kVecBytes;
+  // The streamed tiles arrive in 64-row halves (one sub-step each), so a
+  // stage is released as soon as its sub-step's MMAs complete.
+  static constexpr int kStages = (D == 64) ? 8 : 4;
+  static constexpr uint32_t kTileBytes = kBwdTile * D * 2;  // a stationary 128-row tile
+  static constexpr uint32_t kHalfBytes = kBwdSub * D * 2;   // a streamed 64-row half tile
+  static constexpr uint32_t kHalfBlock = kBwdSub * 128;     // 64 columns x 64 rows
+  static constexpr uint32_t kStageBytes = 2 * kHalfBytes;   // Y0 half, Y1 half
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the swizzle");
+  static constexpr uint32_t kVecBytes = kKV ? 2 * kBwdSub * 4 : 0;  // -LSE2[64], -D[64] per stage
   static constexpr uint32_t kOffX = 0;                // stationary tiles X0, X1
-  static constexpr uint32_t kOffY = 2 * kTileBytes;   // ring of (Y0, Y1[, vectors])
-  static constexpr uint32_t kOffBar = kOffY + kStages * kStageBytes;
+  static constexpr uint32_t kOffY = 2 * kTileBytes;   // ring of (Y0, Y1) halves
+  static constexpr uint32_t kOffVec = kOffY + kStages * kStageBytes;
+  static constexpr uint32_t kOffBar = kOffVec + kStages * kVecBytes;
   // x_full, st_full[2], p_full[2], acc_done, y_full[S], y_empty[S]
   static constexpr int kNumBars = 6 + 2 * kStages;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
@@ -199,6 +213,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // One setmaxnreg per warpgroup, executed by all four of its warps.
+  if (warp < 8) {
+    setmaxnreg_inc<kBwdEwRegs>();
+  } else {
+    setmaxnreg_dec<kBwdControlRegs>();
+  }
+
   if (warp < 8) {
     // ------------------------------------------------------------ elementwise
     const int g = warp >> 2;          // warpgroup = TMEM buffer it serves
@@ -222,18 +243,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int yt = y_first + n;
       const int y0 = yt * kBwdTile + kBwdSub * g;  // first streamed row of this sub-step
       const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdSub > p.N);
-      const float4* vec = reinterpret_cast<const float4*>(
-          smem + C::kOffY + (n % S) * C::kStageBytes + 2 * C::kTileBytes + 4 * kBwdSub * g);
+      const float4* vec =
+          reinterpret_cast<const float4*>(smem + C::kOffVec + (m % S) * C::kVecBytes);
       const uint32_t col_s = C::kColS + kBwdSub * g;
       const uint32_t col_dp = C::kColDP + kBwdSub * g;
+      // All 64 columns of S and dP are loaded before one wait (one TMEM
+      // round trip per sub-step), then processed in two 32-column chunks.
+      uint32_t sr[2][32], dr[2][32];
 #pragma unroll
       for (int cc = 0; cc < kBwdSub / 32; ++cc) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + col_s + 32 * cc, sr);
-        tmem_ld32(tmem + lane_off + col_dp + 32 * cc, dr);
-        tmem_ld_wait();
-        tmem_ld_fence(sr);
-        tmem_ld_fence(dr);
+        tmem_ld32(tmem + lane_off + col_s + 32 * cc, sr[cc]);
+        tmem_ld32(tmem + lane_off + col_dp + 32 * cc, dr[cc]);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < kBwdSub / 32; ++cc) {
+        tmem_ld_fence(sr[cc]);
+        tmem_ld_fence(dr[cc]);
+      }
+#pragma unroll
+      for (int cc = 0; cc < kBwdSub / 32; ++cc) {
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -242,7 +271,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float nl[4], nd[4];
           if (kKV) {
             const float4 a = vec[(32 * cc + e) / 4];
-            const float4 b = vec[(kBwdTile + 32 * cc + e) / 4];
+            const float4 b = vec[(kBwdSub + 32 * cc + e) / 4];
             nl[0] = a.x; nl[1] = a.y; nl[2] = a.z; nl[3] = a.w;
             nd[0] = b.x; nd[1] = b.y; nd[2] = b.z; nd[3] = b.w;
           } else {
@@ -255,8 +284,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int h = 0; h < 4; h += 2) {
             float x0, x1, p0, p1, t0, t1, d0, d1;
-            ffma2(x0, x1, __uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1]), cs, cs,
-                  nl[h], nl[h + 1]);
+            ffma2(x0, x1, __uint_as_float(sr[cc][e + h]), __uint_as_float(sr[cc][e + h + 1]), cs,
+                  cs, nl[h], nl[h + 1]);
             p0 = ex2_approx(x0);
             p1 = ex2_approx(x1);
             if (need_mask) {
@@ -268,15 +297,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (!va) p0 = 0.0f;
               if (!vb) p1 = 0.0f;
             }
-            fadd2(t0, t1, __uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1]), nd[h],
-                  nd[h + 1]);
+            fadd2(t0, t1, __uint_as_float(dr[cc][e + h]), __uint_as_float(dr[cc][e + h + 1]),
+                  nd[h], nd[h + 1]);
             fmul2(d0, d1, p0, p1, t0, t1);
             pp[(e + h) / 2] = pack_bf16x2(p0, p1);
             pd[(e + h) / 2] = pack_bf16x2(d0, d1);
           }
         }
         // Packed pairs of chunk cc land in columns [16cc, 16cc + 16) of the
-        // buffer, which this chunk has already read.
+        // buffer, which have already been read.
         if (kKV) {
           tmem_st16(tmem + lane_off + col_s + 16 * cc, pp);
           tmem_st16(tmem + lane_off + col_dp + 16 * cc, pd);
@@ -333,26 +362,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          xt * kBwdTile, bh, once);
       }
       int issued = 0;
-      for (int n = 0; n < steps; ++n) {
-        const int s = n % S;
-        if (n >= S && !wait_bar(bars.y_empty(s), parity_of(n / S - 1), wctx)) break;
-        const int yt = y_first + n;
+      for (int m = 0; m < 2 * steps; ++m) {
+        const int s = m % S;
+        if (m >= S && !wait_bar(bars.y_empty(s), parity_of(m / S - 1), wctx)) break;
+        const int row0 = (y_first + (m >> 1)) * kBwdTile + kBwdSub * (m & 1);
         const uint32_t stage = sY + s * C::kStageBytes;
-        mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes);
+        mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes + C::kVecBytes);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_3d_hint(stage + b * kSwBlockBytes, &tm_y0, bars.y_full(s), 64 * b,
-                           yt * kBwdTile, bh, keep);
-          tma_load_3d_hint(stage + C::kTileBytes + b * kSwBlockBytes, &tm_y1, bars.y_full(s),
-                           64 * b, yt * kBwdTile, bh, keep);
+          tma_load_3d_hint(stage + b * C::kHalfBlock, &tm_y0, bars.y_full(s), 64 * b, row0, bh, keep);
+          tma_load_3d_hint(stage + C::kHalfBytes + b * C::kHalfBlock, &tm_y1, bars.y_full(s),
+                           64 * b, row0, bh, keep);
         }
         if (kKV) {
-          const size_t v0 = static_cast<size_t>(bh) * p.Npad + yt * kBwdTile;
-          bulk_load(stage + 2 * C::kTileBytes, p.lse2 + v0, kBwdTile * 4, bars.y_full(s));
-          bulk_load(stage + 2 * C::kTileBytes + kBwdTile * 4, p.dvec + v0, kBwdTile * 4,
-                    bars.y_full(s));
+          const size_t v0 = static_cast<size_t>(bh) * p.Npad + row0;
+          const uint32_t vec = sbase + C::kOffVec + s * C::kVecBytes;
+          bulk_load(vec, p.lse2 + v0, kBwdSub * 4, bars.y_full(s));
+          bulk_load(vec + kBwdSub * 4, p.dvec + v0, kBwdSub * 4, bars.y_full(s));
         }
-        issued = n + 1;
+        issued = m + 1;
       }
       // Drain: every copy issued must land before the CTA exits.
       wait_bar_drain(bars.x_full(), 0, wctx);
@@ -363,7 +391,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = elect_one_sync();
     constexpr uint32_t kHi = desc_hi_sw128(1024);
@@ -371,31 +399,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBwdTile, D, 0, 1);
     const uint32_t x_lo = desc_lo(sX, 16);               // X tiles, K-major A
     const uint32_t yk_lo = desc_lo(sY, 16);              // Y tiles, K-major B
-    const uint32_t ymn_lo = desc_lo(sY, kSwBlockBytes);  // Y tiles, MN-major B
+    const uint32_t ymn_lo = desc_lo(sY, C::kHalfBlock);  // Y halves, MN-major B
+    // K-major slice kk of a stationary 128-row tile (16 KB blocks) and of a
+    // streamed 64-row half tile (8 KB blocks).
     auto kmaj_off = [](int kk) -> uint32_t {
       return ((kk >> 2) * kSwBlockBytes + (kk & 3) * 32) >> 4;
+    };
+    auto kmaj_off_half = [](int kk) -> uint32_t {
+      return ((kk >> 2) * C::kHalfBlock + (kk & 3) * 32) >> 4;
     };
     auto commit = [&](uint32_t bar) {
       if (leader) umma_commit(bar);
       __syncwarp();
     };
-    // S and dP of sub-step m (buffer m & 1): X0 and X1 against the 64 rows
-    // 64 (m & 1) .. of the streamed tiles Y0 and Y1 (K-major, 8 KB in).
+    // S and dP of sub-step m (TMEM buffer m & 1, ring stage m % S): X0 and X1
+    // against the 64 streamed rows of Y0 and Y1 in that stage.
     auto issue_sdp = [&](int m) {
       const int b = m & 1;
-      const uint32_t st = ((m >> 1) % S) * C::kStageBytes + b * kBwdSub * 128;
+      const uint32_t st = (m % S) * C::kStageBytes;
       const uint32_t y0 = yk_lo + (st >> 4);
-      const uint32_t y1 = yk_lo + ((st + C::kTileBytes) >> 4);
+      const uint32_t y1 = yk_lo + ((st + C::kHalfBytes) >> 4);
       constexpr uint32_t x1 = C::kTileBytes >> 4;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss_lohi(tmem + C::kColS + kBwdSub * b, x_lo + kmaj_off(kk), kHi,
-                       y0 + kmaj_off(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+                       y0 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss_lohi(tmem + C::kColDP + kBwdSub * b, x_lo + x1 + kmaj_off(kk), kHi,
-                       y1 + kmaj_off(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+                       y1 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
       }
       __syncwarp();
     };
@@ -403,13 +436,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // A operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM buffer m & 1.
     auto issue_acc = [&](int m) {
       const int b = m & 1;
-      const uint32_t st = ((m >> 1) % S) * C::kStageBytes + b * kBwdSub * 128;
+      const uint32_t st = (m % S) * C::kStageBytes;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kBwdSub / 16; ++kk) {
           const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
           const uint32_t r0 = (st + kk * 16 * 128) >> 4;
-          const uint32_t r1 = (st + C::kTileBytes + kk * 16 * 128) >> 4;
+          const uint32_t r1 = (st + C::kHalfBytes + kk * 16 * 128) >> 4;
           if (kKV) {
             umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + kBwdSub * b + 8u * kk,
                          ymn_lo + r1, kHi, kIdescAcc, acc);  // dV += P^T dO
@@ -424,14 +457,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
     };
     const int M = 2 * steps;
-    bool ok = warp_wait_bar(bars.x_full(), 0, wctx) &&
-              warp_wait_bar(bars.y_full(0), 0, wctx);
-    if (ok) {
+    bool ok = warp_wait_bar(bars.x_full(), 0, wctx);
+    for (int m = 0; ok && m < 2; ++m) {
+      if (!warp_wait_bar(bars.y_full(m % S), parity_of(m / S), wctx)) {
+        ok = false;
+        break;
+      }
       tc_fence_after_sync();
-      issue_sdp(0);
-      commit(bars.st_full(0));
-      issue_sdp(1);
-      commit(bars.st_full(1));
+      issue_sdp(m);
+      commit(bars.st_full(m));
     }
     for (int m = 0; ok && m < M; ++m) {
       const int b = m & 1;
@@ -441,19 +475,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_after_sync();
       issue_acc(m);
-      if (b == 1) commit(bars.y_empty((m >> 1) % S));  // both halves of the tile consumed
+      commit(bars.y_empty(m % S));  // this sub-step's half tiles are consumed
       const int m2 = m + 2;
       if (m2 < M) {
         // S, dP of sub-step m + 2 overwrite buffer b after the accumulation
         // that reads it (MMAs of one thread run in issue order).
-        if ((m2 & 1) == 0) {
-          const int n2 = m2 >> 1;
-          if (!warp_wait_bar(bars.y_full(n2 % S), parity_of(n2 / S), wctx)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
+        if (!warp_wait_bar(bars.y_full(m2 % S), parity_of(m2 / S), wctx)) {
+          ok = false;
+          break;
         }
+        tc_fence_after_sync();
         issue_sdp(m2);
         commit(bars.st_full(b));
       }
