@@ -50,11 +50,15 @@ L2_FLUSH_BYTES = 256 << 20
 # per workload (profiles/); the combine pass reads the partials from L2.
 NCU_TRAFFIC_BYTES_DECODE = {
     "decode_b4h16q16k16384d128_causal": 540_661_760,
+    "decode_b4h16q1k16384d128": 539_775_744,
 }
 # Per-launch DRAM traffic of the forward kernel per workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
-NCU_TRAFFIC_BYTES = {}
+NCU_TRAFFIC_BYTES = {
+    "b2h16n4096d128_causal": 130_737_152,
+    "b2h16n4096d256_causal": 571_343_616,
+}
 
 
 def load_peaks():
@@ -197,24 +201,38 @@ def cpu_oracle_sample_decode(w, qkv, heads: int, threads: int = 0, min_seconds: 
     return dt, nbytes, reps, oracle.max_threads() if threads <= 0 else threads
 
 
-def cpu_oracle_sample(w, qkv, rows_per_head: int, seed: int, threads: int = 0):
-    """Time the fp64 oracle on a fixed seeded sample of query rows.
+def cpu_oracle_sample(w, qkv, rows_per_head: int, seed: int, threads: int = 0,
+                      min_seconds: float = 0.0):
+    """Time the fp64 oracle on a fixed seeded sample of query rows (all rows
+    when rows_per_head is 0 or >= N), repeated until min_seconds have passed
+    (at least once).
 
-    Returns (seconds, flops, rows, cores).  FLOPs count the same work the
-    metric counts: 4·d per (query, visible key) pair (2·d for the score,
-    2·d for the P·V row)."""
+    Returns (seconds, flops, rows per head, repetitions, cores).  FLOPs count
+    the same work the metric counts: 4·d per (query, visible key) pair (2·d
+    for the score, 2·d for the P·V row)."""
     import oracle
 
     q, k, v = qkv
-    rng = np.random.Generator(np.random.PCG64(seed))
-    rows = np.sort(rng.permutation(w.N)[:rows_per_head]).astype(np.int64)
-    visible = (rows + 1) if w.causal else np.full(rows.size, w.N)
+    if rows_per_head <= 0 or rows_per_head >= w.N:
+        rows = None
+        idx = np.arange(w.N, dtype=np.int64)
+    else:
+        rng = np.random.Generator(np.random.PCG64(seed))
+        rows = np.sort(rng.permutation(w.N)[:rows_per_head]).astype(np.int64)
+        idx = rows
+    visible = (idx + 1) if w.causal else np.full(idx.size, w.N)
     flops = float(4.0 * w.d * visible.sum() * w.B * w.H)
+    reps = 0
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads,
-                     dtype=getattr(w, "dtype", "bf16"))
-    dt = time.perf_counter() - t0
-    return dt, flops, rows.size, oracle.max_threads() if threads <= 0 else threads
+    while True:
+        oracle.attention(q, k, v, w.causal, w.scale, rows=rows, threads=threads,
+                         dtype=getattr(w, "dtype", "bf16"))
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    cores = oracle.max_threads() if threads <= 0 else threads
+    return dt, flops * reps, idx.size, reps, cores
 
 
 def run_reference(args, w):
@@ -229,7 +247,7 @@ def run_reference(args, w):
     flops = 0.0
     cores = 0
     for i in range(args.warmup + args.steps):
-        dt, flops, n_rows, cores = cpu_oracle_sample(w, qkv, rows_per_head, seed=1000 + w.seed)
+        dt, flops, n_rows, _, cores = cpu_oracle_sample(w, qkv, rows_per_head, seed=1000 + w.seed)
         if i >= args.warmup:
             times.append(dt)
     total = sum(times)
@@ -433,12 +451,13 @@ def run_ours(args, w):
 
         cpu = None
         if world == 1 and not args.skip_cpu_baseline:
-            rows = args.cpu_rows
-            dt, fl, n_rows, cores = cpu_oracle_sample(w, (q, k, v), rows, seed=2000 + w.seed)
+            dt, fl, n_rows, reps, cores = cpu_oracle_sample(
+                w, (q, k, v), args.cpu_rows, seed=2000 + w.seed, min_seconds=args.cpu_seconds)
+            what = ("the whole workload (every row of every head)" if n_rows == w.N else
+                    f"{n_rows} seeded query rows per head x {w.B * w.H} heads "
+                    f"({100.0 * n_rows / w.N:.2f}% of the rows)")
             cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-                   "sample": (f"{n_rows} seeded query rows per head x {w.B * w.H} heads "
-                              f"({100.0 * n_rows / w.N:.2f}% of the rows), fp64 oracle, "
-                              f"{dt:.1f} s")}
+                   "sample": f"{what}, {reps} time(s), fp64 oracle, {dt:.1f} s"}
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
@@ -658,8 +677,10 @@ def main(argv=None):
     ap.add_argument("--workload", default=workloads.HEADLINE.name,
                     choices=[x.name for x in workloads.WORKLOADS + workloads.VARIANT_WORKLOADS
                              + workloads.DECODE_WORKLOADS])
-    ap.add_argument("--cpu-rows", type=int, default=512,
-                    help="query rows per head timed for the CPU baseline")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="query rows per head timed for the CPU baseline (0: all rows, the "
+                         "whole workload, repeated for at least --cpu-seconds)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="query rows per head per step of --impl reference")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
