@@ -29,10 +29,12 @@
 // only key tiles j <= i; the diagonal tile is masked element by element.
 //
 // Each streamed 128-row tile is processed in two 64-row sub-steps whose S
-// and dP live in alternating TMEM buffers, and each buffer has its own
-// warpgroup of elementwise warps: while one warpgroup works on a sub-step,
-// the other works on the next and the tensor core runs the accumulation of
-// the previous one and the S, dP of the one after.  TMEM (512 columns): S
+// and dP live in alternating TMEM buffers, so the tensor core computes the
+// next sub-step's S and dP (and the previous one's accumulation) while the
+// elementwise warps work on the current one.  Both elementwise warpgroups
+// work on every sub-step, warpgroup g on its 32 columns (the latency of a
+// sub-step's elementwise work is on the critical path), and each writes its
+// P/dS pairs into the first half of its own column range.  TMEM (512 columns): S
 // buffers [0,64) and [64,128), dP buffers [128,192) and [192,256), then the
 // accumulators (dK and dV, or dQ), D columns each.  Warps: 0-3 and 4-7
 // elementwise (buffer 0 and 1) and epilogue, 8 the TMA producer, 9 the TMEM
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bars.x_full(), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.st_full(b), 1);
-      mbar_init(bars.p_full(b), 4);  // one arrival per warp of buffer b's warpgroup
+      mbar_init(bars.p_full(b), 8);  // one arrival per elementwise warp
     }
     mbar_init(bars.acc_done(), 1);
     for (int s = 0; s < S; ++s) {
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ elementwise
-    const int g = warp >> 2;          // warpgroup = TMEM buffer it serves
+    const int g = warp >> 2;            // warpgroup: its 32 columns of every sub-step
     const int row = threadIdx.x & 127;  // = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
@@ -233,90 +235,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       nd_r = p.dvec[static_cast<size_t>(bh) * p.Npad + x_idx];
     }
     bool ok = true;
-    for (int m = g; m < 2 * steps; m += 2) {
+    for (int m = 0; m < 2 * steps; ++m) {
+      const int b = m & 1;  // TMEM buffer
       const int n = m >> 1;
-      if (!warp_wait_bar(bars.st_full(g), parity_of(n), wctx)) {
+      if (!warp_wait_bar(bars.st_full(b), parity_of(n), wctx)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       const int yt = y_first + n;
-      const int y0 = yt * kBwdTile + kBwdSub * g;  // first streamed row of this sub-step
-      const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdSub > p.N);
+      const int y0 = yt * kBwdTile + kBwdSub * b + 32 * g;  // first streamed row of these columns
+      const bool need_mask = (p.causal && yt == xt) || (y0 + 32 > p.N);
       const float4* vec =
-          reinterpret_cast<const float4*>(smem + C::kOffVec + (m % S) * C::kVecBytes);
-      const uint32_t col_s = C::kColS + kBwdSub * g;
-      const uint32_t col_dp = C::kColDP + kBwdSub * g;
-      // All 64 columns of S and dP are loaded before one wait (one TMEM
-      // round trip per sub-step), then processed in two 32-column chunks.
-      uint32_t sr[2][32], dr[2][32];
-#pragma unroll
-      for (int cc = 0; cc < kBwdSub / 32; ++cc) {
-        tmem_ld32(tmem + lane_off + col_s + 32 * cc, sr[cc]);
-        tmem_ld32(tmem + lane_off + col_dp + 32 * cc, dr[cc]);
-      }
+          reinterpret_cast<const float4*>(smem + C::kOffVec + (m % S) * C::kVecBytes) + 8 * g;
+      const uint32_t col_s = C::kColS + kBwdSub * b + 32 * g;
+      const uint32_t col_dp = C::kColDP + kBwdSub * b + 32 * g;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + lane_off + col_s, sr);
+      tmem_ld32(tmem + lane_off + col_dp, dr);
       tmem_ld_wait();
+      tmem_ld_fence(sr);
+      tmem_ld_fence(dr);
+      uint32_t pp[16], pd[16];
 #pragma unroll
-      for (int cc = 0; cc < kBwdSub / 32; ++cc) {
-        tmem_ld_fence(sr[cc]);
-        tmem_ld_fence(dr[cc]);
-      }
-#pragma unroll
-      for (int cc = 0; cc < kBwdSub / 32; ++cc) {
-        uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          // -LSE2 and -D of the four columns (kKV: per column, from shared
-          // memory; otherwise this row's).
-          float nl[4], nd[4];
-          if (kKV) {
-            const float4 a = vec[(32 * cc + e) / 4];
-            const float4 b = vec[(kBwdSub + 32 * cc + e) / 4];
-            nl[0] = a.x; nl[1] = a.y; nl[2] = a.z; nl[3] = a.w;
-            nd[0] = b.x; nd[1] = b.y; nd[2] = b.z; nd[3] = b.w;
-          } else {
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              nl[h] = nlse_r;
-              nd[h] = nd_r;
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < 4; h += 2) {
-            float x0, x1, p0, p1, t0, t1, d0, d1;
-            ffma2(x0, x1, __uint_as_float(sr[cc][e + h]), __uint_as_float(sr[cc][e + h + 1]), cs,
-                  cs, nl[h], nl[h + 1]);
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-            if (need_mask) {
-              // key <= query when causal; padding rows past N see nothing.
-              const int ya = y0 + 32 * cc + e + h;
-              const bool va = ya < p.N && (!p.causal || (kKV ? x_idx <= ya : ya <= x_idx));
-              const bool vb = ya + 1 < p.N &&
-                              (!p.causal || (kKV ? x_idx <= ya + 1 : ya + 1 <= x_idx));
-              if (!va) p0 = 0.0f;
-              if (!vb) p1 = 0.0f;
-            }
-            fadd2(t0, t1, __uint_as_float(dr[cc][e + h]), __uint_as_float(dr[cc][e + h + 1]),
-                  nd[h], nd[h + 1]);
-            fmul2(d0, d1, p0, p1, t0, t1);
-            pp[(e + h) / 2] = pack_bf16x2(p0, p1);
-            pd[(e + h) / 2] = pack_bf16x2(d0, d1);
-          }
-        }
-        // Packed pairs of chunk cc land in columns [16cc, 16cc + 16) of the
-        // buffer, which have already been read.
+      for (int e = 0; e < 32; e += 4) {
+        // -LSE2 and -D of the four columns (kKV: per column, from shared
+        // memory; otherwise this row's).
+        float nl[4], nd[4];
         if (kKV) {
-          tmem_st16(tmem + lane_off + col_s + 16 * cc, pp);
-          tmem_st16(tmem + lane_off + col_dp + 16 * cc, pd);
+          const float4 a = vec[e / 4];
+          const float4 c4 = vec[(kBwdSub + e) / 4];
+          nl[0] = a.x; nl[1] = a.y; nl[2] = a.z; nl[3] = a.w;
+          nd[0] = c4.x; nd[1] = c4.y; nd[2] = c4.z; nd[3] = c4.w;
         } else {
-          tmem_st16(tmem + lane_off + col_s + 16 * cc, pd);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            nl[h] = nlse_r;
+            nd[h] = nd_r;
+          }
         }
+#pragma unroll
+        for (int h = 0; h < 4; h += 2) {
+          float x0, x1, p0, p1, t0, t1, d0, d1;
+          ffma2(x0, x1, __uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1]), cs, cs, nl[h],
+                nl[h + 1]);
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
+          if (need_mask) {
+            // key <= query when causal; padding rows past N see nothing.
+            const int ya = y0 + e + h;
+            const bool va = ya < p.N && (!p.causal || (kKV ? x_idx <= ya : ya <= x_idx));
+            const bool vb = ya + 1 < p.N &&
+                            (!p.causal || (kKV ? x_idx <= ya + 1 : ya + 1 <= x_idx));
+            if (!va) p0 = 0.0f;
+            if (!vb) p1 = 0.0f;
+          }
+          fadd2(t0, t1, __uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1]), nd[h],
+                nd[h + 1]);
+          fmul2(d0, d1, p0, p1, t0, t1);
+          pp[(e + h) / 2] = pack_bf16x2(p0, p1);
+          pd[(e + h) / 2] = pack_bf16x2(d0, d1);
+        }
+      }
+      // The pairs go into the first 16 of this warpgroup's 32 columns,
+      // which it has already read.
+      if (kKV) {
+        tmem_st16(tmem + lane_off + col_s, pp);
+        tmem_st16(tmem + lane_off + col_dp, pd);
+      } else {
+        tmem_st16(tmem + lane_off + col_s, pd);
       }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.p_full(g));
+      if (lane == 0) mbar_arrive(bars.p_full(b));
     }
     // ---------------------------------------------------------------- epilogue
     // kKV: warpgroup 0 stores dK (scaled), warpgroup 1 dV; otherwise each
@@ -443,14 +435,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
           const uint32_t r0 = (st + kk * 16 * 128) >> 4;
           const uint32_t r1 = (st + C::kHalfBytes + kk * 16 * 128) >> 4;
+          // Slice kk (16 streamed rows) was packed by warpgroup kk / 2 into
+          // the first 16 of its 32 columns.
+          const uint32_t a_off = kBwdSub * b + 32u * (kk >> 1) + 8u * (kk & 1);
           if (kKV) {
-            umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + kBwdSub * b + 8u * kk,
-                         ymn_lo + r1, kHi, kIdescAcc, acc);  // dV += P^T dO
-            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColDP + kBwdSub * b + 8u * kk,
-                         ymn_lo + r0, kHi, kIdescAcc, acc);  // dK += dS^T Q
+            umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + a_off, ymn_lo + r1, kHi, kIdescAcc,
+                         acc);  // dV += P^T dO
+            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColDP + a_off, ymn_lo + r0, kHi,
+                         kIdescAcc, acc);  // dK += dS^T Q
           } else {
-            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColS + kBwdSub * b + 8u * kk,
-                         ymn_lo + r0, kHi, kIdescAcc, acc);  // dQ += dS K
+            umma_ts_lohi(tmem + C::kColAcc0, tmem + C::kColS + a_off, ymn_lo + r0, kHi, kIdescAcc,
+                         acc);  // dQ += dS K
           }
         }
       }
