@@ -98,7 +98,8 @@ struct BwdCfg {
   static constexpr uint32_t kOffVec = kOffY + kStages * kStageBytes;
   static constexpr uint32_t kOffBar = kOffVec + kStages * kVecBytes;
   // x_full, st_full[2], p_full[2], acc_done, y_full[S], y_empty[S]
-  static constexpr int kNumBars = 6 + 2 * kStages;
+  // ... and x_tmem (query-tile pass: X copied into TMEM)
+  static constexpr int kNumBars = 7 + 2 * kStages;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -108,6 +109,10 @@ struct BwdCfg {
   static constexpr uint32_t kColDP = 128;   // dP buffer b at 128 + 64b; then dS^T (key-tile pass)
   static constexpr uint32_t kColAcc0 = 256;      // dK (key-tile pass) or dQ
   static constexpr uint32_t kColAcc1 = 256 + D;  // dV (key-tile pass)
+  // Query-tile pass: Q_i and dO_i as bf16 pairs in the spare columns, so
+  // the S and dP MMAs read their A operand from TMEM and only K/V from SMEM.
+  static constexpr uint32_t kColXT = 384;
+  static_assert(kKV || kColXT + D <= kTmemCols, "Q and dO pairs fit in TMEM");
 };
 
 struct BwdBars {
@@ -119,6 +124,7 @@ struct BwdBars {
   __device__ uint32_t acc_done() const { return base + 40u; }
   __device__ uint32_t y_full(int s) const { return base + 48u + 8u * s; }
   __device__ uint32_t y_empty(int s) const { return base + 48u + 8u * (stages + s); }
+  __device__ uint32_t x_tmem() const { return base + 48u + 16u * stages; }
 };
 
 // -D_i = -rowsum(dO_i * O_i) and -LSE_i * log2(e) for every row of the
@@ -193,6 +199,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bars.p_full(b), 8);  // one arrival per elementwise warp
     }
     mbar_init(bars.acc_done(), 1);
+    mbar_init(bars.x_tmem(), 8);  // one arrival per elementwise warp
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.y_full(s), 1);
       mbar_init(bars.y_empty(s), 1);
@@ -229,6 +236,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
     const float cs = p.scale_log2;
+    if (!kKV) {
+      // Copy this row of X_g (g = 0: Q_i, 1: dO_i) from the swizzled SMEM
+      // tile into TMEM as bf16 pairs: 16-byte chunk c of the row sits in
+      // 64-column block c / 8 at row * 128 + ((c % 8) ^ (row % 8)) * 16.
+      bool got = warp_wait_bar(bars.x_full(), 0, wctx);
+      if (got) {
+        const uint8_t* xt_s = smem + C::kOffX + g * C::kTileBytes;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 v4 = *reinterpret_cast<const uint4*>(
+                xt_s + h * kSwBlockBytes + row * 128 + (((c8 ^ (row & 7))) << 4));
+            wv[4 * c8] = v4.x;
+            wv[4 * c8 + 1] = v4.y;
+            wv[4 * c8 + 2] = v4.z;
+            wv[4 * c8 + 3] = v4.w;
+          }
+          tmem_st32(tmem + lane_off + C::kColXT + g * (D / 2) + 32 * h, wv);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.x_tmem());
+    }
     float nlse_r = 0.0f, nd_r = 0.0f;
     if (!kKV) {
       nlse_r = p.lse2[static_cast<size_t>(bh) * p.Npad + x_idx];
@@ -413,14 +447,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t y1 = yk_lo + ((st + C::kHalfBytes) >> 4);
       constexpr uint32_t x1 = C::kTileBytes >> 4;
       if (leader) {
+        if (kKV) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lohi(tmem + C::kColS + kBwdSub * b, x_lo + kmaj_off(kk), kHi,
-                       y0 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss_lohi(tmem + C::kColS + kBwdSub * b, x_lo + kmaj_off(kk), kHi,
+                         y0 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss_lohi(tmem + C::kColDP + kBwdSub * b, x_lo + x1 + kmaj_off(kk), kHi,
-                       y1 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss_lohi(tmem + C::kColDP + kBwdSub * b, x_lo + x1 + kmaj_off(kk), kHi,
+                         y1 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+        } else {
+          // A (Q_i, dO_i) from TMEM: 16 columns of the head dimension = 8
+          // TMEM columns of pairs.
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ts_lohi(tmem + C::kColS + kBwdSub * b, tmem + C::kColXT + 8u * kk,
+                         y0 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ts_lohi(tmem + C::kColDP + kBwdSub * b, tmem + C::kColXT + D / 2 + 8u * kk,
+                         y1 + kmaj_off_half(kk), kHi, kIdescSS, kk > 0 ? 1u : 0u);
+        }
       }
       __syncwarp();
     };
@@ -452,7 +499,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
     };
     const int M = 2 * steps;
-    bool ok = warp_wait_bar(bars.x_full(), 0, wctx);
+    // The key-tile pass reads X from SMEM; the query-tile pass from TMEM,
+    // once the elementwise warps have copied it there.
+    bool ok = warp_wait_bar(kKV ? bars.x_full() : bars.x_tmem(), 0, wctx);
     for (int m = 0; ok && m < 2; ++m) {
       if (!warp_wait_bar(bars.y_full(m % S), parity_of(m / S), wctx)) {
         ok = false;
