@@ -31,15 +31,16 @@
 // Each streamed 128-row tile is processed in two 64-row sub-steps whose S
 // and dP live in alternating TMEM buffers, so the tensor core computes the
 // next sub-step's S and dP (and the previous one's accumulation) while the
-// elementwise warps work on the current one.  Both elementwise warpgroups
-// work on every sub-step, warpgroup g on its 32 columns (the latency of a
-// sub-step's elementwise work is on the critical path), and each writes its
-// P/dS pairs into the first half of its own column range.  TMEM (512 columns): S
+// elementwise warps work on the current one.  Four elementwise warpgroups
+// all work on every sub-step, warpgroup g on its 16 columns (the latency of
+// a sub-step's elementwise work is on the critical path), and each writes
+// its P/dS pairs into the first half of its own column range, which is
+// exactly the TMEM A operand of one 16-row accumulation MMA.  TMEM (512 columns): S
 // buffers [0,64) and [64,128), dP buffers [128,192) and [192,256), then the
-// accumulators (dK and dV, or dQ), D columns each.  Warps: 0-3 and 4-7
-// elementwise (buffer 0 and 1) and epilogue, 8 the TMA producer, 9 the TMEM
-// allocator and MMA issuer, 10-11 idle.  Every wait is bounded like the
-// forward's (status word, drain, TMEM freed).
+// accumulators (dK and dV, or dQ), D columns each.  Warps: 0-15 elementwise
+// and epilogue, 16 the TMA producer, 17 the TMEM allocator and MMA issuer,
+// 18-19 idle.  Every wait is bounded like the forward's (status word, drain,
+// TMEM freed).
 #pragma once
 
 #include <cstdint>
@@ -51,20 +52,23 @@
 
 namespace fa {
 
-// Three warpgroups: two elementwise, one with the producer, the MMA issuer
-// and two idle warps.  Launched with 168 registers a thread (65536 / 384,
-// rounded to what three warps per sub-partition allow); setmaxnreg then
-// moves registers from the control warpgroup to the elementwise ones.
-constexpr int kBwdThreads = 384;
-constexpr int kBwdLoadWarp = 8;
-constexpr int kBwdMmaWarp = 9;
-constexpr uint32_t kBwdLaunchRegs = 168;
-constexpr uint32_t kBwdEwRegs = 200;
-constexpr uint32_t kBwdControlRegs = 104;
-static_assert(2 * 128 * kBwdEwRegs + 128 * kBwdControlRegs <= kBwdThreads * kBwdLaunchRegs,
+// Five warpgroups: four elementwise, one with the producer, the MMA issuer
+// and two idle warps.  Launched with 96 registers a thread (five warps per
+// sub-partition); setmaxnreg then moves registers from the control
+// warpgroup to the elementwise ones.
+constexpr int kBwdEwGroups = 4;
+constexpr int kBwdThreads = (kBwdEwGroups + 1) * 128;
+constexpr int kBwdLoadWarp = 4 * kBwdEwGroups;
+constexpr int kBwdMmaWarp = kBwdLoadWarp + 1;
+constexpr uint32_t kBwdLaunchRegs = 96;
+constexpr uint32_t kBwdEwRegs = 104;
+constexpr uint32_t kBwdControlRegs = 56;
+static_assert(kBwdEwGroups * 128 * kBwdEwRegs + 128 * kBwdControlRegs <=
+                  kBwdThreads * kBwdLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kBwdTile = 128;  // rows of every tile (keys or queries)
 constexpr int kBwdSub = 64;    // streamed rows per sub-step
+constexpr int kBwdEwCols = kBwdSub / 4;  // columns of a sub-step per elementwise warpgroup
 
 struct BwdParams {
   uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][D] bf16
@@ -196,10 +200,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bars.x_full(), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.st_full(b), 1);
-      mbar_init(bars.p_full(b), 8);  // one arrival per elementwise warp
+      mbar_init(bars.p_full(b), 4 * kBwdEwGroups);  // one arrival per elementwise warp
     }
     mbar_init(bars.acc_done(), 1);
-    mbar_init(bars.x_tmem(), 8);  // one arrival per elementwise warp
+    mbar_init(bars.x_tmem(), 4 * kBwdEwGroups);  // one arrival per elementwise warp
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.y_full(s), 1);
       mbar_init(bars.y_empty(s), 1);
@@ -223,24 +227,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // One setmaxnreg per warpgroup, executed by all four of its warps.
-  if (warp < 8) {
+  if (warp < 4 * kBwdEwGroups) {
     setmaxnreg_inc<kBwdEwRegs>();
   } else {
     setmaxnreg_dec<kBwdControlRegs>();
   }
 
-  if (warp < 8) {
+  if (warp < 4 * kBwdEwGroups) {
     // ------------------------------------------------------------ elementwise
-    const int g = warp >> 2;            // warpgroup: its 32 columns of every sub-step
+    const int g = warp >> 2;            // warpgroup: its 16 columns of every sub-step
     const int row = threadIdx.x & 127;  // = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
     const float cs = p.scale_log2;
     if (!kKV) {
-      // Copy this row of X_g (g = 0: Q_i, 1: dO_i) from the swizzled SMEM
+      // Warpgroups 0 and 1 copy this row of X_g (g = 0: Q_i, 1: dO_i) from the swizzled SMEM
       // tile into TMEM as bf16 pairs: 16-byte chunk c of the row sits in
       // 64-column block c / 8 at row * 128 + ((c % 8) ^ (row % 8)) * 16.
-      bool got = warp_wait_bar(bars.x_full(), 0, wctx);
+      bool got = g < 2 && warp_wait_bar(bars.x_full(), 0, wctx);
       if (got) {
         const uint8_t* xt_s = smem + C::kOffX + g * C::kTileBytes;
 #pragma unroll
@@ -278,21 +282,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_after_sync();
       const int yt = y_first + n;
-      const int y0 = yt * kBwdTile + kBwdSub * b + 32 * g;  // first streamed row of these columns
-      const bool need_mask = (p.causal && yt == xt) || (y0 + 32 > p.N);
-      const float4* vec =
-          reinterpret_cast<const float4*>(smem + C::kOffVec + (m % S) * C::kVecBytes) + 8 * g;
-      const uint32_t col_s = C::kColS + kBwdSub * b + 32 * g;
-      const uint32_t col_dp = C::kColDP + kBwdSub * b + 32 * g;
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lane_off + col_s, sr);
-      tmem_ld32(tmem + lane_off + col_dp, dr);
+      const int y0 = yt * kBwdTile + kBwdSub * b + kBwdEwCols * g;  // first streamed row here
+      const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdEwCols > p.N);
+      const float4* vec = reinterpret_cast<const float4*>(smem + C::kOffVec + (m % S) * C::kVecBytes) +
+                          (kBwdEwCols / 4) * g;
+      const uint32_t col_s = C::kColS + kBwdSub * b + kBwdEwCols * g;
+      const uint32_t col_dp = C::kColDP + kBwdSub * b + kBwdEwCols * g;
+      uint32_t sr[kBwdEwCols], dr[kBwdEwCols];
+      tmem_ld16(tmem + lane_off + col_s, sr);
+      tmem_ld16(tmem + lane_off + col_dp, dr);
       tmem_ld_wait();
-      tmem_ld_fence(sr);
-      tmem_ld_fence(dr);
-      uint32_t pp[16], pd[16];
+      tmem_ld_fence16(sr);
+      tmem_ld_fence16(dr);
+      uint32_t pp[kBwdEwCols / 2], pd[kBwdEwCols / 2];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
+      for (int e = 0; e < kBwdEwCols; e += 4) {
         // -LSE2 and -D of the four columns (kKV: per column, from shared
         // memory; otherwise this row's).
         float nl[4], nd[4];
@@ -331,13 +335,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pd[(e + h) / 2] = pack_bf16x2(d0, d1);
         }
       }
-      // The pairs go into the first 16 of this warpgroup's 32 columns,
-      // which it has already read.
+      // The pairs go into the first 8 of this warpgroup's 16 columns, which
+      // it has already read: the A operand of accumulation slice g.
       if (kKV) {
-        tmem_st16(tmem + lane_off + col_s, pp);
-        tmem_st16(tmem + lane_off + col_dp, pd);
+        tmem_st8(tmem + lane_off + col_s, pp);
+        tmem_st8(tmem + lane_off + col_dp, pd);
       } else {
-        tmem_st16(tmem + lane_off + col_s, pd);
+        tmem_st8(tmem + lane_off + col_s, pd);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -345,31 +349,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(bars.p_full(b));
     }
     // ---------------------------------------------------------------- epilogue
-    // kKV: warpgroup 0 stores dK (scaled), warpgroup 1 dV; otherwise each
-    // warpgroup stores half of dQ's columns (scaled).
+    // kKV: warpgroups 0 and 1 store the two column halves of dK (scaled), 2
+    // and 3 those of dV; otherwise each warpgroup stores a quarter of dQ's
+    // columns (scaled).
     if (ok && warp_wait_bar(bars.acc_done(), 0, wctx)) {
       tc_fence_after_sync();
       const bool in_range = x_idx < p.N;
-      constexpr int kCols = kKV ? D : D / 2;
-      const uint32_t col = kKV ? (g == 0 ? C::kColAcc0 : C::kColAcc1) : C::kColAcc0 + kCols * g;
-      const float mul = (kKV && g == 1) ? 1.0f : p.scale;
-      uint16_t* out = (kKV && g == 1) ? p.out1 : p.out0;
+      constexpr int kCols = kKV ? D / 2 : D / 4;
+      const int part = kKV ? (g & 1) : g;
+      const bool is_dv = kKV && g >= 2;
+      const uint32_t col = (is_dv ? C::kColAcc1 : C::kColAcc0) + kCols * part;
+      const float mul = is_dv ? 1.0f : p.scale;
+      uint16_t* out = is_dv ? p.out1 : p.out0;
       uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * D +
-                                            (kKV ? 0 : kCols * g));
+                                            kCols * part);
 #pragma unroll
-      for (int cc = 0; cc < kCols / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + col + 32 * cc, r);
+      for (int cc = 0; cc < kCols / 16; ++cc) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_off + col + 16 * cc, r);
         tmem_ld_wait();
-        tmem_ld_fence(r);
+        tmem_ld_fence16(r);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 2; ++q4) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             w4[e] = pack_bf16x2(__uint_as_float(r[8 * q4 + 2 * e]) * mul,
                                 __uint_as_float(r[8 * q4 + 2 * e + 1]) * mul);
-          if (in_range) dst[4 * cc + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          if (in_range) dst[2 * cc + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
     }
@@ -482,9 +489,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
           const uint32_t r0 = (st + kk * 16 * 128) >> 4;
           const uint32_t r1 = (st + C::kHalfBytes + kk * 16 * 128) >> 4;
-          // Slice kk (16 streamed rows) was packed by warpgroup kk / 2 into
-          // the first 16 of its 32 columns.
-          const uint32_t a_off = kBwdSub * b + 32u * (kk >> 1) + 8u * (kk & 1);
+          // Slice kk (16 streamed rows) was packed by warpgroup kk into the
+          // first 8 of its 16 columns.
+          const uint32_t a_off = kBwdSub * b + kBwdEwCols * kk;
           if (kKV) {
             umma_ts_lohi(tmem + C::kColAcc1, tmem + C::kColS + a_off, ymn_lo + r1, kHi, kIdescAcc,
                          acc);  // dV += P^T dO
