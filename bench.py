@@ -428,13 +428,15 @@ def run_ours(args, w):
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peaks_src} hbm_gbs",
-                         "timed": "split pass and combine pass together, per step",
+                         "timed": "the whole split-KV call (one or two launches), per step",
                          "traffic": NCU_TRAFFIC_BYTES_DECODE.get(w.name)},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": DECODE_UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "ms_per_step": e2e_ms / e2e_steps},
-            "gpu_launches": 2 * args.steps,  # split pass + combine pass per step
+            # one clustered launch per step when the ranges fit in a cluster
+            # (<= 8), else the split pass and the combine pass
+            "gpu_launches": (1 if n_splits <= 8 else 2) * args.steps,
             "launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
                           "max": max(per_launch_ms)},
             "clocks": clocks,

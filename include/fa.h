@@ -110,10 +110,13 @@ int fa_fwd_strided(const void *q, const int64_t *q_strides, const void *k,
  * aligned to the end of the keys: query i (0 <= i < Nq) sees keys
  * 0 .. Nk - Nq + i (for Nq == Nk this is fa_fwd's rule).  The keys are cut
  * into contiguous ranges, each range's attention (a normalised output and its
- * log-sum-exp) is computed into `workspace`, and the ranges are merged with
- * the block-merge identity ("Parsing FlashAttention (2)" eq. (20); "Online
- * Softmax and FlashAttention", course unit 12):
+ * log-sum-exp) is computed, and the ranges are merged with the block-merge
+ * identity ("Parsing FlashAttention (2)" eq. (20); "Online Softmax and
+ * FlashAttention", course unit 12):
  *     LSE = ln sum_s e^(LSE_s),   O = sum_s e^(LSE_s - LSE) O_s.
+ * With at most 8 ranges the ranges of a (batch, head) run as one thread-block
+ * cluster and merge on chip (one launch, workspace untouched); otherwise the
+ * partials go through `workspace` and a second launch merges them.
  *
  *   q         : const bf16 [B][H][Nq][d] (device, 16-byte aligned)
  *   k, v      : const bf16 [B][H][Nk][d] (device, 16-byte aligned)

@@ -97,7 +97,11 @@ cudaError_t configure_order_kernel() {
 
 template <int D>
 cudaError_t configure_split_kernel() {
-  return cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(fa::SplitCfg<D>::kSmemAlloc));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fa::fa_splitkv_partial_kernel<D, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::SplitCfg<D>::kSmemAlloc));
 }
@@ -608,11 +612,33 @@ int current_sms() {
   return sms;
 }
 
+// Largest cluster the split pass uses (portable cluster size).
+constexpr int kMaxClusterSplits = 8;
+
+// The split pass, then the merge: on chip in one clustered launch when the
+// ranges of a batch*head fit in one cluster (and `allow_cluster`), else
+// through the workspace and the combine kernel.
 template <int D>
 int launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const fa::SplitParams& prm,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, bool allow_cluster) {
   const dim3 grid1(static_cast<unsigned>(prm.splits), static_cast<unsigned>(prm.num_bh));
-  fa::fa_splitkv_partial_kernel<D>
+  if (allow_cluster && prm.splits <= kMaxClusterSplits) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid1;
+    cfg.blockDim = dim3(fa::kSplitThreads);
+    cfg.dynamicSmemBytes = fa::SplitCfg<D>::kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(prm.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fa::fa_splitkv_partial_kernel<D, true>, mk, mv, prm);
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  }
+  fa::fa_splitkv_partial_kernel<D, false>
       <<<grid1, fa::kSplitThreads, fa::SplitCfg<D>::kSmemAlloc, stream>>>(mk, mv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   const unsigned rows = static_cast<unsigned>(prm.num_bh * prm.Nq);
@@ -698,7 +724,7 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_split<64>(mk, mv, prm, s) : launch_split<128>(mk, mv, prm, s);
+  return d == 64 ? launch_split<64>(mk, mv, prm, s, true) : launch_split<128>(mk, mv, prm, s, true);
 }
 
 // ----------------------------------------------------------------------------
@@ -796,7 +822,9 @@ extern "C" int fa_fwd_splitkv_static(const void* q, const void* k, const void* v
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_split<64>(mk, mv, prm, s) : launch_split<128>(mk, mv, prm, s);
+  // Always the two-pass form: this entry point's partials go through its
+  // built-in scratch array.
+  return d == 64 ? launch_split<64>(mk, mv, prm, s, false) : launch_split<128>(mk, mv, prm, s, false);
 }
 
 extern "C" const char* fa_strerror(int code) {

@@ -23,12 +23,24 @@
 // a multiprocessor; the host picks the split count so that all CTAs run in
 // one wave when the batch allows.
 //
-// Waits are bounded like those of the main kernel (status word, no hang).
+// With at most 8 key ranges (the common decode case) the ranges of one
+// (batch, head) are launched as one thread-block cluster (kCluster) and
+// merged on chip instead: each CTA leaves its normalised partial output and
+// log-sum-exp in its own shared memory, the cluster synchronises, each CTA
+// merges a share of the output elements reading the others' partials
+// through distributed shared memory, and a second cluster barrier keeps
+// every partial alive until all reads are done.  No workspace and no second
+// launch.
+//
+// Waits are bounded like those of the main kernel (status word, no hang);
+// every CTA of a cluster reaches both cluster barriers, also after a
+// timed-out wait.
 #pragma once
 
 #include <climits>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "fa_fwd_kernel.cuh"  // g_fa_status, kStatusTimeout
@@ -61,8 +73,10 @@ struct SplitCfg {
   static constexpr uint32_t kTileBytes = kSplitTileKeys * D * 2;  // K (or V) tile: D/64 boxes
   static constexpr uint32_t kStageBytes = 2 * kTileBytes;         // K then V
   static constexpr uint32_t kOffBar = kStages * kStageBytes;
-  // The warp merge reuses the ring: O [warps][16][D], then m and l [warps][16].
-  static constexpr uint32_t kMergeBytes = kSplitConsumerWarps * kSplitMaxQ * (D + 2) * 4;
+  // The warp merge reuses the ring: O [warps][16][D], then m and l
+  // [warps][16], then the range's partial O [16][D] and LSE [16].
+  static constexpr uint32_t kMergeBytes =
+      kSplitConsumerWarps * kSplitMaxQ * (D + 2) * 4 + kSplitMaxQ * (D + 1) * 4;
   static_assert(kMergeBytes <= kOffBar, "merge area fits in the ring");
   static constexpr uint32_t kSmemBytes = kOffBar + 2 * kStages * 8;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // 1024-byte alignment for SW128
@@ -89,8 +103,33 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
                                (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// Pass 1: one CTA per (split, batch*head).
-template <int D>
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Pass 1: one CTA per (split, batch*head); with kCluster, the CTAs of one
+// batch*head form a cluster and also do pass 2.
+template <int D, bool kCluster>
 __global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
     fa_splitkv_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
@@ -276,53 +315,96 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
   // ------------------------------------------------------------ merge warps
   const bool all_ok = __syncthreads_and(ok);
   const size_t row_base = (static_cast<size_t>(split) * p.num_bh + bh) * Nq;
-  if (!all_ok) {
-    for (int idx = threadIdx.x; idx < Nq * D; idx += kSplitThreads) {
-      p.ws_o[row_base * D + idx] = 0.0f;
-      if (idx % D == 0) p.ws_lse[row_base + idx / D] = -CUDART_INF_F;
-    }
-    return;
-  }
-  // Every issued tile was consumed, so no copy is in flight: reuse the ring.
+  // Partial result of this range: normalised O_s and LSE_s (natural log),
+  // to the workspace or (kCluster) to this CTA's shared memory after the
+  // warp-merge area.
   float* os = reinterpret_cast<float*>(smem);                           // [warp][16][D]
   float* ms = os + kSplitConsumerWarps * kSplitMaxQ * D;                // [warp][16]
   float* ls = ms + kSplitConsumerWarps * kSplitMaxQ;                    // [warp][16]
-  if (warp < kSplitConsumerWarps) {
-#pragma unroll
-    for (int n = 0; n < kNTiles; ++n) {
-      float* r0 = os + (warp * kSplitMaxQ + g) * D + 8 * n + 2 * t4;
-      float* r1 = r0 + 8 * D;
-      *reinterpret_cast<float2*>(r0) = make_float2(acc[n][0], acc[n][1]);
-      *reinterpret_cast<float2*>(r1) = make_float2(acc[n][2], acc[n][3]);
+  float* part_o = ls + kSplitConsumerWarps * kSplitMaxQ;                // [16][D]
+  float* part_lse = part_o + kSplitMaxQ * D;                            // [16]
+  auto put = [&](int i, int col, float o, float lse) {
+    if (kCluster) {
+      part_o[i * D + col] = o;
+      if (col == 0) part_lse[i] = lse;
+    } else {
+      p.ws_o[(row_base + i) * D + col] = o;
+      if (col == 0) p.ws_lse[row_base + i] = lse;
     }
-    if (t4 == 0) {
-      ms[warp * kSplitMaxQ + g] = m0;
-      ms[warp * kSplitMaxQ + g + 8] = m1;
-      ls[warp * kSplitMaxQ + g] = l0;
-      ls[warp * kSplitMaxQ + g + 8] = l1;
-    }
-  }
-  __syncthreads();
-  // One thread per (query, column): merge the warps, normalise, write.
-  for (int idx = threadIdx.x; idx < Nq * D; idx += kSplitThreads) {
-    const int i = idx / D;
-    const int col = idx % D;
-    float m = -CUDART_INF_F;
+  };
+  if (!all_ok) {
+    for (int idx = threadIdx.x; idx < Nq * D; idx += kSplitThreads)
+      put(idx / D, idx % D, 0.0f, -CUDART_INF_F);
+  } else {
+    // Every issued tile was consumed, so no copy is in flight: reuse the ring.
+    if (warp < kSplitConsumerWarps) {
 #pragma unroll
-    for (int w = 0; w < kSplitConsumerWarps; ++w) m = fmaxf(m, ms[w * kSplitMaxQ + i]);
-    float l = 0.0f, o = 0.0f;
-    if (m != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < kSplitConsumerWarps; ++w) {
-        const float mw = ms[w * kSplitMaxQ + i];
-        const float e = mw == -CUDART_INF_F ? 0.0f : ex2_approx(mw - m);
-        l += e * ls[w * kSplitMaxQ + i];
-        o += e * os[(w * kSplitMaxQ + i) * D + col];
+      for (int n = 0; n < kNTiles; ++n) {
+        float* r0 = os + (warp * kSplitMaxQ + g) * D + 8 * n + 2 * t4;
+        float* r1 = r0 + 8 * D;
+        *reinterpret_cast<float2*>(r0) = make_float2(acc[n][0], acc[n][1]);
+        *reinterpret_cast<float2*>(r1) = make_float2(acc[n][2], acc[n][3]);
+      }
+      if (t4 == 0) {
+        ms[warp * kSplitMaxQ + g] = m0;
+        ms[warp * kSplitMaxQ + g + 8] = m1;
+        ls[warp * kSplitMaxQ + g] = l0;
+        ls[warp * kSplitMaxQ + g + 8] = l1;
       }
     }
-    const bool any = l > 0.0f;
-    p.ws_o[(row_base + i) * D + col] = any ? o / l : 0.0f;
-    if (col == 0) p.ws_lse[row_base + i] = any ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+    __syncthreads();
+    // One thread per (query, column): merge the warps, normalise, write.
+    for (int idx = threadIdx.x; idx < Nq * D; idx += kSplitThreads) {
+      const int i = idx / D;
+      const int col = idx % D;
+      float m = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < kSplitConsumerWarps; ++w) m = fmaxf(m, ms[w * kSplitMaxQ + i]);
+      float l = 0.0f, o = 0.0f;
+      if (m != -CUDART_INF_F) {
+#pragma unroll
+        for (int w = 0; w < kSplitConsumerWarps; ++w) {
+          const float mw = ms[w * kSplitMaxQ + i];
+          const float e = mw == -CUDART_INF_F ? 0.0f : ex2_approx(mw - m);
+          l += e * ls[w * kSplitMaxQ + i];
+          o += e * os[(w * kSplitMaxQ + i) * D + col];
+        }
+      }
+      const bool any = l > 0.0f;
+      put(i, col, any ? o / l : 0.0f, any ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F);
+    }
+  }
+  if (kCluster) {
+    // Pass 2 on chip: CTA `rank` merges output elements rank, rank + S*T, ...
+    // of this batch*head from the partials of all S ranges (block merge,
+    // as in fa_splitkv_combine_kernel).
+    cluster_sync_all();
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t nr = static_cast<uint32_t>(p.splits);
+    const uint32_t po = smem_u32(part_o), pl = smem_u32(part_lse);
+    for (int idx = static_cast<int>(rank) * kSplitThreads + threadIdx.x; idx < Nq * D;
+         idx += static_cast<int>(nr) * kSplitThreads) {
+      const int i = idx / D;
+      const int col = idx % D;
+      float m = -CUDART_INF_F;
+      for (uint32_t s2 = 0; s2 < nr; ++s2)
+        m = fmaxf(m, ld_cluster_f32(cluster_map(pl + 4u * i, s2)));
+      float total = 0.0f, o = 0.0f;
+      if (m != -CUDART_INF_F) {
+        for (uint32_t s2 = 0; s2 < nr; ++s2) {
+          const float ls2 = ld_cluster_f32(cluster_map(pl + 4u * i, s2));
+          if (ls2 == -CUDART_INF_F) continue;  // no visible key in that range
+          const float w = __expf(ls2 - m);
+          total += w;
+          o = fmaf(w, ld_cluster_f32(cluster_map(po + 4u * (i * D + col), s2)), o);
+        }
+      }
+      const size_t orow = static_cast<size_t>(bh) * Nq + i;
+      const float inv = total > 0.0f ? 1.0f / total : 0.0f;
+      reinterpret_cast<__nv_bfloat16*>(p.o)[orow * D + col] = __float2bfloat16_rn(o * inv);
+      if (col == 0) p.lse[orow] = m + __logf(total);
+    }
+    cluster_sync_all();  // the other CTAs' partials stay alive until here
   }
 }
 
