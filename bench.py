@@ -46,12 +46,10 @@ DECODE_UNIT = "GB/s"
 BWD_METRIC = "attention bwd TFLOPS (nominal 2.5x forward FLOPs) & % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-# DRAM bytes (read + write) of one split-pass launch, from one ncu capture
-# per workload (profiles/); the combine pass reads the partials from L2.
-NCU_TRAFFIC_BYTES_DECODE = {
-    "decode_b4h16q16k16384d128_causal": 540_661_760,
-    "decode_b4h16q1k16384d128": 539_775_744,
-}
+# DRAM bytes (read + write) of one split-KV call (the clustered split pass),
+# from one ncu capture per workload (profiles/); a workload is left out
+# until a capture of the kernel as benchmarked exists.
+NCU_TRAFFIC_BYTES_DECODE = {}
 # Per-launch DRAM traffic of the forward kernel per workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
