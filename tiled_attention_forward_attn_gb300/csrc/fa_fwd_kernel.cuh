@@ -515,9 +515,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ok = false;
             break;
           }
+          mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_4d_hint(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s),
+                             64 * b, j * kBlockN, u.h, u.b, keep);
+          ++kc;
           if (j == 0) {
             // Q_t of this unit replaces the previous unit's once every S_t
-            // MMA that read it has completed (q_empty).
+            // MMA that read it has completed (q_empty).  K_0 goes first: it
+            // does not wait for the previous unit's last S MMAs.
 #pragma unroll
             for (int t = 0; t < kTilesPerCta; ++t) {
               if (!ok || u.n[t] == 0) continue;
@@ -534,12 +541,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             if (!ok) break;
           }
-          mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
-#pragma unroll
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_4d_hint(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s),
-                             64 * b, j * kBlockN, u.h, u.b, keep);
-          ++kc;
         }
       }
       // Drain: every copy issued must land before the CTA may exit.  The last
