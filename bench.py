@@ -54,7 +54,6 @@ NCU_TRAFFIC_BYTES_DECODE = {}
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
-    "b2h16n4096d128_causal": 130_737_152,
     "b2h16n4096d256_causal": 571_343_616,
 }
 

@@ -18,10 +18,11 @@
 // tiles stream in while the current unit finishes.  Three warpgroups:
 //   warps 0-3   softmax and epilogue of tile A; thread t owns row t = TMEM lane t
 //   warps 4-7   softmax and epilogue of tile B
-//   warp 8      TMA producer of Q_A, Q_B and the K_j ring
+//   warp 8      TMA producer of Q_A, Q_B and of one K/V ring that it fills
+//               in the order the MMAs read it: K_0, then V_j, K_j+1 per key
+//               tile (each tile is prefetched about two iterations ahead)
 //   warp 9      TMEM allocator and the tcgen05.mma issuer
-//   warp 10     TMA producer of the V_j ring
-//   warp 11     idle (it completes the third warpgroup)
+//   warps 10-11 idle (they complete the third warpgroup)
 // The third warpgroup hands most of its registers to the two softmax
 // warpgroups (setmaxnreg): 384 threads launch with 168 registers each
 // (64512 in all); afterwards 256 x 200 + 128 x 104 = 64512 are in use.
@@ -81,9 +82,8 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kNumThreads * kLaun
               "register split exceeds the launch allocation");
 static_assert(2 * kSoftmaxRegs + kControlRegs <= 512, "per-sub-partition register file");
 constexpr int kRowThreadsPerTile = 128;
-constexpr int kLoadWarp = 8;    // Q and K producer
-constexpr int kMmaWarp = 9;
-constexpr int kLoadVWarp = 10;  // V producer
+constexpr int kLoadWarp = 8;  // Q, K and V producer
+constexpr int kMmaWarp = 9;   // warps 10 and 11 only fill the third warpgroup
 constexpr uint32_t kSwBlockBytes = 128 * 128;  // [128 rows x 64 bf16] swizzled block
 constexpr float kRescaleThreshold = 8.0f;      // log2 units: P stays <= 2^8
 
@@ -113,19 +113,19 @@ struct FwdParams {
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension");
-  // Ring depths: 64 KB of Q plus 3 K and 2 V tiles of 32 KB fill 224 KB at
-  // D = 128; at D = 64 the tiles are half as large.
-  static constexpr int kStagesK = (D == 64) ? 4 : 3;
-  static constexpr int kStagesV = (D == 64) ? 4 : 2;
+  // One ring of K and V tiles, filled and drained in the order the MMAs
+  // use them (K_0, then V_j, K_j+1 for each key tile j): 64 KB of Q plus 5
+  // slots of 32 KB fill 224 KB at D = 128; at D = 64 the tiles are half as
+  // large.
+  static constexpr int kSlots = (D == 64) ? 8 : 5;
   static constexpr uint32_t kQBytes = kTileM * D * 2;  // one query tile
   static constexpr uint32_t kKVBytes = kBlockN * D * 2;
   static constexpr uint32_t kOffQ = 0;  // Q_A, Q_B
-  static constexpr uint32_t kOffK = kOffQ + kTilesPerCta * kQBytes;
-  static constexpr uint32_t kOffV = kOffK + kStagesK * kKVBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStagesV * kKVBytes;
+  static constexpr uint32_t kOffRing = kOffQ + kTilesPerCta * kQBytes;
+  static constexpr uint32_t kOffBar = kOffRing + kSlots * kKVBytes;
   // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, p_half[2],
-  // k_full[SK], k_empty[SK], v_full[SV], v_empty[SV]
-  static constexpr int kNumBars = 13 + 2 * kStagesK + 2 * kStagesV;
+  // kv_full[R], kv_empty[R]
+  static constexpr int kNumBars = 13 + 2 * kSlots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -138,7 +138,7 @@ struct Cfg {
 // Barrier addresses (8 bytes each) in the order of the layout above.
 struct Barriers {
   uint32_t base;
-  int sk, sv;  // K and V ring depths
+  int slots;  // K/V ring depth
   __device__ uint32_t q_full(int t) const { return base + 8u * t; }
   __device__ uint32_t q_empty(int t) const { return base + 16u + 8u * t; }
   __device__ uint32_t s_full(int t) const { return base + 32u + 8u * t; }
@@ -146,10 +146,8 @@ struct Barriers {
   __device__ uint32_t o_done(int t) const { return base + 64u + 8u * t; }
   __device__ uint32_t mma_done() const { return base + 80u; }
   __device__ uint32_t p_half(int t) const { return base + 88u + 8u * t; }
-  __device__ uint32_t k_full(int s) const { return base + 104u + 8u * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 104u + 8u * (sk + s); }
-  __device__ uint32_t v_full(int s) const { return base + 104u + 8u * (2 * sk + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 104u + 8u * (2 * sk + sv + s); }
+  __device__ uint32_t kv_full(int s) const { return base + 104u + 8u * s; }
+  __device__ uint32_t kv_empty(int s) const { return base + 104u + 8u * (slots + s); }
 };
 
 struct WaitCtx {
@@ -419,18 +417,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = Cfg<D>;
-  constexpr int SK = C::kStagesK;
-  constexpr int SV = C::kStagesV;
+  constexpr int R = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::kOffQ;
-  const uint32_t sK = sbase + C::kOffK;
-  const uint32_t sV = sbase + C::kOffV;
+  const uint32_t sRing = sbase + C::kOffRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
-  const Barriers bars{sbase + C::kOffBar, SK, SV};
+  const Barriers bars{sbase + C::kOffBar, R};
   const WaitCtx wctx{abort_flag, p.wait_limit_ns};
 
   const int warp = threadIdx.x >> 5;
@@ -446,13 +442,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.mma_done(), 1);
-    for (int s = 0; s < SK; ++s) {
-      mbar_init(bars.k_full(s), 1);
-      mbar_init(bars.k_empty(s), 1);
-    }
-    for (int s = 0; s < SV; ++s) {
-      mbar_init(bars.v_full(s), 1);
-      mbar_init(bars.v_empty(s), 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(bars.kv_full(s), 1);
+      mbar_init(bars.kv_empty(s), 1);
     }
     *abort_flag = 0u;
     fence_barrier_init();
@@ -494,105 +486,78 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         break;
     }
   } else if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ Q, K producer
+    // ------------------------------------------------------------ Q, K, V producer
     if (lane == 0) {
       // K/V tiles are read again by every query unit of the same head: keep
       // them in L2.  Q is read once.
       const uint64_t keep = make_l2_policy_evict_last();
       const uint64_t once = make_l2_policy_evict_first();
-      uint32_t kc = 0;                     // K tiles issued so far (ring position)
+      uint32_t ic = 0;                     // K/V items issued (or skipped) so far
       uint32_t qc[kTilesPerCta] = {0, 0};  // Q tiles issued so far, per tile slot
+      int64_t skipped = -1;                // test hook: the item never issued
+      bool v_seen = false;
+      int cur_h = 0, cur_b = 0;
+      // One K or V tile into the next ring slot, once that slot is free.
+      auto issue = [&](const CUtensorMap* map, int row0, bool skip) -> bool {
+        const int s = static_cast<int>(ic % R);
+        if (ic >= static_cast<uint32_t>(R) &&
+            !wait_bar(bars.kv_empty(s), parity_of(ic / R - 1), wctx))
+          return false;
+        if (skip) {
+          skipped = ic;
+        } else {
+          mbar_arrive_expect_tx(bars.kv_full(s), C::kKVBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_4d_hint(sRing + s * C::kKVBytes + b * kSwBlockBytes, map, bars.kv_full(s),
+                             64 * b, row0, cur_h, cur_b, keep);
+        }
+        ++ic;
+        return true;
+      };
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int idx = unit_index(r);
         if (idx >= p.total_units) break;
         const Unit u = unit_at(idx, p);
+        cur_h = u.h;
+        cur_b = u.b;
         const int n_max = max(u.n[0], u.n[1]);
-        for (int j = 0; j < n_max; ++j) {
-          const int s = static_cast<int>(kc % SK);
-          if (kc >= static_cast<uint32_t>(SK) &&
-              !wait_bar(bars.k_empty(s), parity_of(kc / SK - 1), wctx)) {
+        if (!issue(&tm_k, 0, false)) break;  // K_0 does not wait for the Q slots
+        // Q_t of this unit replaces the previous unit's once every S_t MMA
+        // that read it has completed (q_empty).
+#pragma unroll
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          if (!ok || u.n[t] == 0) continue;
+          if (qc[t] > 0 && !wait_bar(bars.q_empty(t), parity_of(qc[t] - 1), wctx)) {
             ok = false;
-            break;
+            continue;
           }
-          mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
+          mbar_arrive_expect_tx(bars.q_full(t), C::kQBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
-            tma_load_4d_hint(sK + s * C::kKVBytes + b * kSwBlockBytes, &tm_k, bars.k_full(s),
-                             64 * b, j * kBlockN, u.h, u.b, keep);
-          ++kc;
-          if (j == 0) {
-            // Q_t of this unit replaces the previous unit's once every S_t
-            // MMA that read it has completed (q_empty).  K_0 goes first: it
-            // does not wait for the previous unit's last S MMAs.
-#pragma unroll
-            for (int t = 0; t < kTilesPerCta; ++t) {
-              if (!ok || u.n[t] == 0) continue;
-              if (qc[t] > 0 && !wait_bar(bars.q_empty(t), parity_of(qc[t] - 1), wctx)) {
-                ok = false;
-                continue;
-              }
-              mbar_arrive_expect_tx(bars.q_full(t), C::kQBytes);
-#pragma unroll
-              for (int b = 0; b < D / 64; ++b)
-                tma_load_4d_hint(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t),
-                                 64 * b, u.q0 + kTileM * t, u.h, u.b, once);
-              ++qc[t];
-            }
-            if (!ok) break;
-          }
+            tma_load_4d_hint(sQ + t * C::kQBytes + b * kSwBlockBytes, &tm_q, bars.q_full(t),
+                             64 * b, u.q0 + kTileM * t, u.h, u.b, once);
+          ++qc[t];
+        }
+        for (int j = 0; ok && j < n_max; ++j) {
+          const bool skip = !v_seen && (p.inject & kInjectSkipFirstV);
+          v_seen = true;
+          if (!issue(&tm_v, j * kBlockN, skip) ||
+              (j + 1 < n_max && !issue(&tm_k, (j + 1) * kBlockN, false)))
+            ok = false;
         }
       }
       // Drain: every copy issued must land before the CTA may exit.  The last
-      // copy into stage s is the largest count < kc congruent to s mod SK.
+      // item in slot s is the largest count < ic congruent to s mod R.
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t)
         if (qc[t] > 0) wait_bar_drain(bars.q_full(t), parity_of(qc[t] - 1), wctx);
-#pragma unroll
-      for (int s = 0; s < SK; ++s) {
-        if (kc > static_cast<uint32_t>(s)) {
-          const uint32_t last = kc - 1 - ((kc - 1 - s) % SK);
-          wait_bar_drain(bars.k_full(s), parity_of(last / SK), wctx);
-        }
-      }
-    }
-  } else if (warp == kLoadVWarp) {
-    // ------------------------------------------------------------ V producer
-    if (lane == 0) {
-      const uint64_t keep = make_l2_policy_evict_last();
-      uint32_t vc = 0;  // V tiles issued (or deliberately skipped) so far
-      bool v0_skipped = false;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int idx = unit_index(r);
-        if (idx >= p.total_units) break;
-        const Unit u = unit_at(idx, p);
-        const int n_max = max(u.n[0], u.n[1]);
-        for (int j = 0; j < n_max; ++j) {
-          const int s = static_cast<int>(vc % SV);
-          if (vc >= static_cast<uint32_t>(SV) &&
-              !wait_bar(bars.v_empty(s), parity_of(vc / SV - 1), wctx)) {
-            ok = false;
-            break;
-          }
-          ++vc;
-          if (vc == 1 && (p.inject & kInjectSkipFirstV)) {
-            v0_skipped = true;
-            continue;
-          }
-          mbar_arrive_expect_tx(bars.v_full(s), C::kKVBytes);
-#pragma unroll
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_4d_hint(sV + s * C::kKVBytes + b * kSwBlockBytes, &tm_v, bars.v_full(s),
-                             64 * b, j * kBlockN, u.h, u.b, keep);
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < SV; ++s) {
-        if (vc > static_cast<uint32_t>(s)) {
-          const uint32_t last = vc - 1 - ((vc - 1 - s) % SV);
-          if (!(last == 0 && v0_skipped))
-            wait_bar_drain(bars.v_full(s), parity_of(last / SV), wctx);
+      for (int s = 0; s < R; ++s) {
+        if (ic > static_cast<uint32_t>(s)) {
+          const uint32_t last = ic - 1 - ((ic - 1 - s) % R);
+          if (static_cast<int64_t>(last) != skipped)
+            wait_bar_drain(bars.kv_full(s), parity_of(last / R), wctx);
         }
       }
     }
@@ -614,8 +579,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // low halves of all descriptors are a base plus compile-time offsets.
     constexpr uint32_t kHi = desc_hi_sw128(1024);
     const uint32_t q_lo = desc_lo(sQ, 16);
-    const uint32_t k_lo = desc_lo(sK, 16);
-    const uint32_t v_lo = desc_lo(sV, kSwBlockBytes);
+    const uint32_t k_lo = desc_lo(sRing, 16);             // K slots, K-major
+    const uint32_t v_lo = desc_lo(sRing, kSwBlockBytes);  // V slots, MN-major
     // K-major slice kk of a [128 x D] tile: block kk/4, 32 bytes per slice.
     auto kmaj_off = [](int kk) -> uint32_t {
       return ((kk >> 2) * kSwBlockBytes + (kk & 3) * 32) >> 4;
@@ -654,7 +619,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       __syncwarp();
     };
 
-    uint32_t kc = 0, vc = 0;             // ring positions consumed
+    uint32_t ic = 0;                     // K/V items consumed (ring position)
     uint32_t qc[kTilesPerCta] = {0, 0};  // Q loads consumed per tile slot
     uint32_t pc[kTilesPerCta] = {0, 0};  // p_full phases consumed per tile
     bool ok = true;
@@ -667,7 +632,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const Unit u = unit_at(idx, p);
       const int n_max = max(u.n[0], u.n[1]);
       // j = 0: S_t(0) for every active tile.
-      if (!warp_wait_bar(bars.k_full(kc % SK), parity_of(kc / SK), wctx)) break;
+      if (!warp_wait_bar(bars.kv_full(ic % R), parity_of(ic / R), wctx)) break;
+      const uint32_t k0_slot = ic % R;
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t) {
         if (!ok || u.n[t] == 0) continue;
@@ -676,17 +642,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           continue;
         }
         ++qc[t];
-        issue_s(t, kc % SK);
+        issue_s(t, k0_slot);
         commit(bars.s_full(t));
         if (u.n[t] == 1) commit(bars.q_empty(t));  // last S_t of the unit
       }
       if (!ok) break;
-      commit(bars.k_empty(kc % SK));
-      ++kc;
+      commit(bars.kv_empty(k0_slot));
+      ++ic;
       for (int j = 0; ok && j < n_max; ++j) {
         const bool more = j + 1 < n_max;
-        if (!warp_wait_bar(bars.v_full(vc % SV), parity_of(vc / SV), wctx) ||
-            (more && !warp_wait_bar(bars.k_full(kc % SK), parity_of(kc / SK), wctx))) {
+        // Items ic (V_j) and ic + 1 (K_j+1, when there is one).
+        const uint32_t v_slot = ic % R, k_slot = (ic + 1) % R;
+        if (!warp_wait_bar(bars.kv_full(v_slot), parity_of(ic / R), wctx) ||
+            (more && !warp_wait_bar(bars.kv_full(k_slot), parity_of((ic + 1) / R), wctx))) {
           ok = false;
           break;
         }
@@ -699,20 +667,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             continue;
           }
           tc_fence_after_sync();
-          issue_pv(t, vc % SV, j == 0, 0);
+          issue_pv(t, v_slot, j == 0, 0);
           if (!warp_wait_bar(bars.p_full(t), parity_of(pc[t]), wctx)) {
             ok = false;
             continue;
           }
           ++pc[t];
           tc_fence_after_sync();
-          issue_pv(t, vc % SV, j == 0, 1);
+          issue_pv(t, v_slot, j == 0, 1);
           // V_j is free once the last tile that reads it has its P.V issued
           // (released before the S MMA that follows, to refill the ring early).
-          if (t == kTilesPerCta - 1 || j >= u.n[kTilesPerCta - 1]) commit(bars.v_empty(vc % SV));
+          if (t == kTilesPerCta - 1 || j >= u.n[kTilesPerCta - 1]) commit(bars.kv_empty(v_slot));
           if (j + 1 < n) {
             // S_t(j+1) overwrites P_t(j); MMAs of one thread run in issue order.
-            issue_s(t, kc % SK);
+            issue_s(t, k_slot);
             commit(bars.s_full(t));  // also covers P_t(j) V_j: O_t is current
             if (j + 2 == n) commit(bars.q_empty(t));  // last S_t of the unit
           } else {
@@ -720,10 +688,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
         }
         if (!ok) break;
-        ++vc;
+        ++ic;  // V_j
         if (more) {
-          commit(bars.k_empty(kc % SK));  // K_j+1: every S MMA issued
-          ++kc;
+          commit(bars.kv_empty(k_slot));  // K_j+1: every S MMA issued
+          ++ic;
         }
       }
     }
