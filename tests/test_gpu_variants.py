@@ -187,3 +187,40 @@ def test_overlapping_output_rows_rejected(fa, cuda_device):
     with pytest.raises(fa.FAError) as err:
         fa.fa_fwd(q, q, q, o, lse, False, 0.1)
     assert err.value.code == 13
+
+
+def _growing_scores(B, H, N, d, seed, dtype):
+    """Scores that jump up in the middle of key tiles: the scaled scores
+    (base-2 exponent units) of head 0 rise by about 20 on keys 320..383 (the
+    second half of key tile 2) and by about 20 more on keys 384..447 (the
+    first half of key tile 3); those of head 1 climb by 4 to 6 every 64 keys.
+    So a half tile's P sum against the reference of the keys before it
+    exceeds 2^15 in either half of a key tile: the reference moves mid-tile
+    as well as at tile starts."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    k = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    v = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    q[..., 0] = 4.0
+    k[..., 0] = 0.0
+    k[:, 0, 320:384, 0] = 40.0
+    k[:, 0, 384:448, 0] = 80.0
+    if H > 1:
+        k[:, 1, :, 0] = 8.0 * (np.arange(N) // 64)
+    conv = workloads.f32_to_f16_bits if dtype == "f16" else workloads.f32_to_bf16_bits
+    return conv(q), conv(k), conv(v)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_reference_moves_mid_tile(fa, cuda_device, d, causal, dtype):
+    """Rows whose maximum grows inside a key tile (second half) and at the
+    first half of the next, so the exponent reference moves after the first
+    half of P has been handed over: the result is still the oracle's."""
+    N = 1000
+    scale = 0.125 if d == 64 else 1.0 / math.sqrt(d)
+    q, k, v = _growing_scores(1, 2, N, d, seed=690 + d, dtype=dtype)
+    o, lse = _run(fa, cuda_device, q, k, v, causal, scale, dtype)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, scale, dtype=dtype)
+    compare(o, lse, o_ref, lse_ref, label=f"moving reference d{d} c{causal} {dtype}")

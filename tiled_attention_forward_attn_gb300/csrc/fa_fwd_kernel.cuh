@@ -41,10 +41,12 @@
 // of the next unit overwrites O_t only after the softmax warps, which read
 // O_t in their epilogue, have handed over that unit's first P_t.
 //
-// Rescaling is lazy: the exponent reference m_ref of a row only moves when a
-// tile's maximum exceeds it by more than 8 (base-2 exponent units), so P, l
-// and O keep sharing one reference and the result is unchanged; most tiles
-// then need no O rescale at all.
+// Rescaling is lazy and needs no row maximum on most tiles: each half of P
+// is computed against the row's current exponent reference m_ref, and the
+// reference moves (to the true maximum, with O and l rescaled) only when a
+// half's P sum exceeds 2^15, i.e. when some P could leave the fp16 range;
+// the first tile of a row always sets it.  P, l and O keep sharing one reference, so
+// the result is that of any other reference.
 //
 // Element types and shapes: Q, K, V and O are bf16 or fp16 (kF16; both MMA
 // operands always share the type, P included), the accumulation and the
@@ -86,6 +88,9 @@ constexpr int kLoadWarp = 8;  // Q, K and V producer
 constexpr int kMmaWarp = 9;   // warps 10 and 11 only fill the third warpgroup
 constexpr uint32_t kSwBlockBytes = 128 * 128;  // [128 rows x 64 bf16] swizzled block
 constexpr float kRescaleThreshold = 8.0f;      // log2 units: P stays <= 2^8
+// A half tile's P sum above 2^15 moves the reference: at or below it every P
+// is <= 2^15, inside the fp16 range (max 65504) and far inside bf16's.
+constexpr float kPSumLimit = 32768.0f;
 
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kInjectSkipFirstV = 1u;  // test hook: never issue the first V load
@@ -124,8 +129,8 @@ struct Cfg {
   static constexpr uint32_t kOffRing = kOffQ + kTilesPerCta * kQBytes;
   static constexpr uint32_t kOffBar = kOffRing + kSlots * kKVBytes;
   // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, p_half[2],
-  // kv_full[R], kv_empty[R]
-  static constexpr int kNumBars = 13 + 2 * kSlots;
+  // kv_full[R], kv_empty[R], pv_half[2]
+  static constexpr int kNumBars = 15 + 2 * kSlots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -148,6 +153,8 @@ struct Barriers {
   __device__ uint32_t p_half(int t) const { return base + 88u + 8u * t; }
   __device__ uint32_t kv_full(int s) const { return base + 104u + 8u * s; }
   __device__ uint32_t kv_empty(int s) const { return base + 104u + 8u * (slots + s); }
+  // Completion of the P.V MMAs of the first 64 keys of tile t's current key tile.
+  __device__ uint32_t pv_half(int t) const { return base + 104u + 8u * (2 * slots + t); }
 };
 
 struct WaitCtx {
@@ -296,46 +303,14 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
         if (i > lim) s[i] = masked;
     }
 
-    // Row extreme of the raw scores (max for a positive scale, min for a
-    // negative one), eight independent chains.  (The three-input min/max
-    // forms of sm_100+ were dropped: inside this kernel they produced NaN for
-    // some register allocations, while two-input chains are exact.)
-    float ev[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) ev[k] = s[k];
-#pragma unroll
-    for (int i = 8; i < kBlockN; i += 8)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ev[k] = kNegScale ? fminf(ev[k], s[i + k]) : fmaxf(ev[k], s[i + k]);
-#pragma unroll
-    for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-      for (int k = 0; k < w; ++k) ev[k] = kNegScale ? fminf(ev[k], ev[k + w]) : fmaxf(ev[k], ev[k + w]);
-    const float ext = ev[0];
-    const float m_tile = ext * c;  // max of the scaled scores of this tile
-
-    // Lazy rescale: move the reference only when the tile max exceeds it by
-    // more than the threshold (always on the first tile, where m_ref = -inf).
-    const bool rescale = __any_sync(0xffffffffu, m_tile > m_ref + kRescaleThreshold);
-    float alpha = 1.0f;
-    if (rescale) {
-      const float m_new = fmaxf(m_ref, m_tile);
-      alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
-      l_run *= alpha;
-      m_ref = m_new;
-    }
-
     // P = 2^(s*c - m_ref) and its row sum; P_t goes, as 16-bit pairs, over the
     // first 64 columns of S_t (whose values are already in registers), in
-    // two halves of 64 keys so that half of the scores are dead before the
-    // second.  Each half is handed over on its own (p_half, then p_full):
-    // the P.V MMAs of the first 64 keys start while the second half of P is
-    // still being computed.
-    const float neg_m = -m_ref;
+    // two halves of 64 keys, each handed over on its own (p_half, then
+    // p_full): the P.V MMAs of the first 64 keys start while the second half
+    // of P is still being computed.
     float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t pk[32];
+    uint32_t pk[32];
+    auto exps_half = [&](int h, float neg_m) {
 #pragma unroll
       for (int i = 0; i < 64; i += 4) {
         const int e = 64 * h + i;
@@ -349,32 +324,107 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
         pk[i / 2] = pack_x2<kF16>(p0, p1);
         pk[i / 2 + 1] = pack_x2<kF16>(p2, p3);
       }
-      tmem_st32(s_addr + 32 * h, pk);
-      if (h == 0 && rescale && j > 0) {
-        // O_t holds every P.V product up to tile j-1 (the S_t(j) MMA was
-        // committed after them) and no MMA touches it until p_half: rescale
-        // it in place, before the first half of P is handed over.
+    };
+    // Row extreme of the raw scores over keys [lo, hi) (max for a positive
+    // scale, min for a negative one), eight two-input chains, scaled by c:
+    // the max of the scaled scores.  (The three-input min/max forms of
+    // sm_100+ are not used: inside this kernel they produced NaN for some
+    // register allocations, while two-input chains are exact.)
+    auto scaled_extreme = [&](int lo, int hi) -> float {
+      float ev[8];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + 32 * cc, o);
-          tmem_ld_wait();
-          tmem_ld_fence(o);
+      for (int k = 0; k < 8; ++k) ev[k] = s[lo + k];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a0, a1;
-            fmul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-            o[i] = __float_as_uint(a0);
-            o[i + 1] = __float_as_uint(a1);
-          }
-          tmem_st32(o_addr + 32 * cc, o);
+      for (int i = lo + 8; i < hi; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          ev[k] = kNegScale ? fminf(ev[k], s[i + k]) : fmaxf(ev[k], s[i + k]);
+#pragma unroll
+      for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k)
+          ev[k] = kNegScale ? fminf(ev[k], ev[k + w]) : fmaxf(ev[k], ev[k + w]);
+      return ev[0] * c;
+    };
+    // Moves the reference up to m_new (>= m_ref): the sums so far and, when
+    // O_t already holds products of earlier tiles, O_t itself are scaled by
+    // alpha = 2^(m_ref - m_new) so that everything shares one reference.
+    auto rescale_o = [&](float alpha) {
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + 32 * cc, o);
+        tmem_ld_wait();
+        tmem_ld_fence(o);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float a0, a1;
+          fmul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+          o[i] = __float_as_uint(a0);
+          o[i + 1] = __float_as_uint(a1);
         }
+        tmem_st32(o_addr + 32 * cc, o);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(h == 0 ? bars.p_half(t) : bars.p_full(t));
+    };
+
+    // Lazy reference: each half of P is first computed against the current
+    // reference m_ref, with no row maximum at all.  A half whose P sum stays
+    // at or below 2^15 has every P <= 2^15, which the 16-bit P (bf16 or
+    // fp16) and the fp32 sums hold with the same relative precision as
+    // P <= 1, so it is kept; the result is the same for any reference.  Only
+    // when a half's sum exceeds the limit (or is not finite), and always on
+    // the first tile, where m_ref = -inf, is the reference moved to the true
+    // maximum and the half computed again.
+    //   First half: nothing has been handed over yet, so the reference moves
+    //   for the whole tile (extreme of all 128 keys).
+    bool moved = j == 0;
+    if (!moved) {
+      exps_half(0, -m_ref);
+      moved = __any_sync(0xffffffffu, !((sa0 + sa1) + (sb0 + sb1) <= kPSumLimit));
     }
+    if (moved) {
+      const float m_new = fmaxf(m_ref, scaled_extreme(0, kBlockN));
+      const float alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
+      l_run *= alpha;
+      m_ref = m_new;
+      sa0 = sa1 = sb0 = sb1 = 0.f;
+      exps_half(0, -m_ref);
+      tmem_st32(s_addr, pk);
+      // O_t holds every P.V product up to tile j-1 (the S_t(j) MMA was
+      // committed after them) and no MMA touches it until p_half: rescale
+      // it in place, before the first half of P is handed over.
+      if (j > 0) rescale_o(alpha);
+    } else {
+      tmem_st32(s_addr, pk);
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bars.p_half(t));
+    l_run += (sa0 + sa1) + (sb0 + sb1);
+
+    //   Second half: after a move above every P of the tile is <= 1.  If the
+    //   sum still exceeds the limit, the first half is already in the P.V
+    //   MMAs: wait for them (pv_half), move the reference to the extreme of
+    //   the second half, rescale O_t and the running sum, recompute.
+    sa0 = sa1 = sb0 = sb1 = 0.f;
+    exps_half(1, -m_ref);
+    if (__any_sync(0xffffffffu, !((sa0 + sa1) + (sb0 + sb1) <= kPSumLimit))) {
+      const float m_new = fmaxf(m_ref, scaled_extreme(kBlockN / 2, kBlockN));
+      const float alpha = ex2_approx(m_ref - m_new);
+      l_run *= alpha;
+      m_ref = m_new;
+      sa0 = sa1 = sb0 = sb1 = 0.f;
+      exps_half(1, -m_ref);
+      if (!warp_wait_bar(bars.pv_half(t), parity_of(s_uses - 1), wctx)) return false;
+      tc_fence_after_sync();
+      rescale_o(alpha);
+    }
+    tmem_st32(s_addr + 32, pk);
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bars.p_full(t));
     l_run += (sa0 + sa1) + (sb0 + sb1);
   }
 
@@ -439,6 +489,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.s_full(t), 1);
       mbar_init(bars.p_full(t), kRowThreadsPerTile / 32);  // one arrival per warp
       mbar_init(bars.p_half(t), kRowThreadsPerTile / 32);
+      mbar_init(bars.pv_half(t), 1);
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.mma_done(), 1);
@@ -668,6 +719,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           tc_fence_after_sync();
           issue_pv(t, v_slot, j == 0, 0);
+          commit(bars.pv_half(t));
           if (!warp_wait_bar(bars.p_full(t), parity_of(pc[t]), wctx)) {
             ok = false;
             continue;
