@@ -224,3 +224,24 @@ def test_reference_moves_mid_tile(fa, cuda_device, d, causal, dtype):
     o, lse = _run(fa, cuda_device, q, k, v, causal, scale, dtype)
     o_ref, lse_ref = oracle.attention(q, k, v, causal, scale, dtype=dtype)
     compare(o, lse, o_ref, lse_ref, label=f"moving reference d{d} c{causal} {dtype}")
+
+
+@pytest.mark.parametrize("offset,pad", [(0, 8), (8, 16)])
+def test_output_rows_16_byte_aligned_only(fa, cuda_device, offset, pad):
+    """O rows that are 16-byte but not 32-byte aligned (row stride d + 8
+    elements, or the whole output shifted by 8 elements): the epilogue falls
+    back to 16-byte stores, and the columns around each row stay untouched."""
+    import torch
+
+    B, H, N, d = 1, 2, 300, 128
+    q, k, v = workloads.generate_shape(B, H, N, d, seed=720 + offset)
+    qd, kd, vd = (workloads.as_torch(a).to(cuda_device) for a in (q, k, v))
+    big = torch.full((B, H, N, offset + d + pad), 5.0, dtype=torch.bfloat16, device=cuda_device)
+    o = big[..., offset:offset + d]
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=cuda_device)
+    fa.fa_fwd(qd, kd, vd, o, lse, True, 0.09)
+    torch.cuda.synchronize(cuda_device)
+    assert bool((big[..., :offset] == 5.0).all()) and bool((big[..., offset + d:] == 5.0).all())
+    o_ref, lse_ref = oracle.attention(q, k, v, True, 0.09)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
+            label=f"o offset {offset} pad {pad}")

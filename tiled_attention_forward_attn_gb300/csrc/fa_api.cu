@@ -317,6 +317,10 @@ int fwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* 
   prm.o_sb = os[0];
   prm.o_sh = os[1];
   prm.o_sn = os[2];
+  prm.o_vec32 = (reinterpret_cast<uintptr_t>(o) % 32 == 0 && os[0] % 16 == 0 && os[1] % 16 == 0 &&
+                 os[2] % 16 == 0)
+                    ? 1
+                    : 0;
   prm.N = N;
   prm.H = H;
   prm.d = d;

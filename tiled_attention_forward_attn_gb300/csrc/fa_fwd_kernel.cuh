@@ -113,6 +113,7 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e); never 0 (scale 0 arrives as a tiny positive value)
   uint32_t inject;   // test hooks (0 in normal use)
   uint64_t wait_limit_ns;
+  int o_vec32 = 0;   // 1: O's base and strides are 32-byte multiples (32-byte row stores)
 };
 
 template <int D>
@@ -430,31 +431,40 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
 
   // ---------------------------------------------------------------- epilogue
   // O = O_t / l in the element type, straight from registers to global
-  // memory (each thread writes its own row, 2*d contiguous bytes), then LSE.
+  // memory: each thread writes its own row, 2*d contiguous bytes, in 32-byte
+  // stores where O's alignment allows (16-byte ones otherwise).  All of O_t
+  // is read from TMEM with a single wait.
   if (!warp_wait_bar(bars.o_done(t), parity_of(o_uses), wctx)) return false;
   ++o_uses;
   tc_fence_after_sync();
   const float inv_l = 1.0f / l_run;
   const bool in_range = q_idx < p.N;
-  uint4* dst = reinterpret_cast<uint4*>(p.o + u.b * p.o_sb + u.h * p.o_sh + q_idx * p.o_sn);
+  uint32_t ov[D];
 #pragma unroll
-  for (int cc = 0; cc < D / 32; ++cc) {
-    uint32_t o[32];
-    tmem_ld32(o_addr + 32 * cc, o);
-    tmem_ld_wait();
-    tmem_ld_fence(o);
+  for (int cc = 0; cc < D / 32; ++cc)
+    tmem_ld32(o_addr + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&ov[32 * cc]));
+  tmem_ld_wait();
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t w4[4];
+  for (int cc = 0; cc < D / 32; ++cc) tmem_ld_fence(*reinterpret_cast<uint32_t(*)[32]>(&ov[32 * cc]));
+  uint32_t w[D / 2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float a0, a1;
-        fmul2(a0, a1, __uint_as_float(o[8 * g + 2 * e]), __uint_as_float(o[8 * g + 2 * e + 1]),
-              inv_l, inv_l);
-        w4[e] = pack_x2<kF16>(a0, a1);
-      }
-      if (in_range && (!kPartialD || 32 * cc + 8 * g < p.d))
-        dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  for (int i = 0; i < D / 2; ++i) {
+    float a0, a1;
+    fmul2(a0, a1, __uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1]), inv_l, inv_l);
+    w[i] = pack_x2<kF16>(a0, a1);
+  }
+  if (in_range) {
+    uint16_t* row = p.o + u.b * p.o_sb + u.h * p.o_sh + q_idx * p.o_sn;
+    if (p.o_vec32) {
+#pragma unroll
+      for (int g = 0; g < D / 16; ++g)
+        if (!kPartialD || 16 * g < p.d) st_global_v8(row + 16 * g, &w[8 * g]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(row);
+#pragma unroll
+      for (int g = 0; g < D / 8; ++g)
+        if (!kPartialD || 8 * g < p.d)
+          dst[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
     }
   }
   if (in_range)
