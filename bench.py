@@ -49,11 +49,15 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) of one split-KV call (the clustered split pass),
 # from one ncu capture per workload (profiles/); a workload is left out
 # until a capture of the kernel as benchmarked exists.
-NCU_TRAFFIC_BYTES_DECODE = {}
+NCU_TRAFFIC_BYTES_DECODE = {
+    "decode_b4h16q16k16384d128_causal": 540_464_384,
+    "decode_b4h16q1k16384d128": 538_349_056,
+}
 # Per-launch DRAM traffic of the forward kernel per workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
+    "b2h16n4096d128_causal": 140_705_280,
     "b2h16n4096d256_causal": 571_343_616,
 }
 
