@@ -213,7 +213,7 @@ def _growing_scores(B, H, N, d, seed, dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_reference_moves_mid_tile(fa, cuda_device, d, causal, dtype):
     """Rows whose maximum grows inside a key tile (second half) and at the
     first half of the next, so the exponent reference moves after the first
@@ -226,14 +226,15 @@ def test_reference_moves_mid_tile(fa, cuda_device, d, causal, dtype):
     compare(o, lse, o_ref, lse_ref, label=f"moving reference d{d} c{causal} {dtype}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("offset,pad", [(0, 8), (8, 16)])
-def test_output_rows_16_byte_aligned_only(fa, cuda_device, offset, pad):
+def test_output_rows_16_byte_aligned_only(fa, cuda_device, offset, pad, d):
     """O rows that are 16-byte but not 32-byte aligned (row stride d + 8
     elements, or the whole output shifted by 8 elements): the epilogue falls
     back to 16-byte stores, and the columns around each row stay untouched."""
     import torch
 
-    B, H, N, d = 1, 2, 300, 128
+    B, H, N = 1, 2, 300
     q, k, v = workloads.generate_shape(B, H, N, d, seed=720 + offset)
     qd, kd, vd = (workloads.as_torch(a).to(cuda_device) for a in (q, k, v))
     big = torch.full((B, H, N, offset + d + pad), 5.0, dtype=torch.bfloat16, device=cuda_device)

@@ -1,28 +1,39 @@
 // Fused attention forward for head dimension 256 on sm_103a: the method of
 // fa_fwd_kernel.cuh (tiled online softmax, "Q/O stay, K/V move", causal
-// tiles past the diagonal skipped, lazy rescale, one division at the end),
-// laid out for a 256-column accumulator.
+// tiles past the diagonal skipped, lazy exponent reference, one division at
+// the end), laid out for a 256-column accumulator.
 //
 // Two query tiles per CTA would need 2 x (128 + 256) TMEM columns, more than
 // the 512 there are, so a work unit is one 128-row query tile and the
 // tensor core is kept busy by double-buffering S instead: keys come in
 // 64-key tiles, S(j) lives in one of two 64-column TMEM buffers, and while
-// the softmax warps turn S(j) into P(j) the tensor core computes S(j+1) and
-// then P(j-1) V(j-1).  TMEM: S buffers [0,64) and [64,128), O [256,512).
-// SMEM: Q 64 KB, a 3-stage K ring and a 2-stage V ring of 32 KB tiles.
+// the softmax warps turn S(j) into P(j) the tensor core computes P(j-1) V
+// and S(j+1).
+//
+// Q lives in TMEM too, as 16-bit pairs (128 columns): S = Q K^T is then a
+// TS-form MMA that reads only K (2 KB per 128x64x16 step) from shared
+// memory, at the tensor core's full rate; with Q in shared memory too the
+// 64-key product is bound by shared-memory bandwidth (6 KB per step, 48
+// instead of 32 cycles).  The softmax warps copy each unit's Q from the
+// swizzled shared-memory tile into TMEM once its last S MMA of the previous
+// unit has completed, before that unit's epilogue, so the next unit's first
+// S MMAs overlap the epilogue.
+//
+// TMEM: S buffers [0,64) and [64,128) (P as 16-bit pairs over the first 32
+// columns of its buffer), Q [128,256), O [256,512).  SMEM: the Q staging
+// tile (64 KB) and one ring of five 32 KB K/V tiles filled in the order the
+// MMAs read them (K_0, K_1, then V_j, K_j+2).
 //
 // pv_done completes one phase per P.V.  A parity wait is only meaningful
 // while the waiter is at most one phase behind, so the softmax warps
-// confirm the previous tile's P.V on every tile (at the rescale point, or
-// just before handing over P; the P.V after that cannot start earlier).
+// confirm the previous tile's P.V on every tile (when the reference moves,
+// or just before handing over P; the P.V after that cannot start earlier).
 //
-// Warps: 0-3 softmax and epilogue (thread = row = TMEM lane), 4 TMA producer
-// of Q and K, 5 TMEM allocator and MMA issuer, 6 TMA producer of V, 7 idle.
-// The persistent grid walks (batch*head, query tile) units heaviest first in
-// a serpentine, like the main kernel.  O is rescaled in place only when the
-// reference max moves (rare); before that the softmax warps wait for the
-// previous P.V to complete (pv_done).  Every wait is bounded (status word,
-// drain, TMEM freed).
+// Warps: 0-3 softmax, Q copy and epilogue (thread = row = TMEM lane), 4 TMA
+// producer of Q and the K/V ring, 5 TMEM allocator and MMA issuer, 6-7
+// idle.  The persistent grid walks (batch*head, query tile) units heaviest
+// first in a serpentine, like the main kernel.  Every wait is bounded
+// (status word, drain, TMEM freed).
 #pragma once
 
 #include <cstdint>
@@ -38,8 +49,8 @@ constexpr int kW_TileM = 128;   // query rows per unit
 constexpr int kW_BlockN = 64;   // keys per K/V tile
 constexpr int kW_D = 256;
 constexpr int kW_Threads = 256;
-constexpr int kW_LoadWarp = 4, kW_MmaWarp = 5, kW_LoadVWarp = 6;
-constexpr int kW_StagesK = 3, kW_StagesV = 2;
+constexpr int kW_LoadWarp = 4, kW_MmaWarp = 5;
+constexpr int kW_Slots = 5;     // K/V ring depth
 
 struct WideCfg {
   static constexpr uint32_t kQBlock = kW_TileM * 128;   // 64 columns x 128 rows
@@ -47,17 +58,17 @@ struct WideCfg {
   static constexpr uint32_t kQBytes = kW_TileM * kW_D * 2;   // 64 KB
   static constexpr uint32_t kKVBytes = kW_BlockN * kW_D * 2;  // 32 KB
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kQBytes;
-  static constexpr uint32_t kOffV = kOffK + kW_StagesK * kKVBytes;
-  static constexpr uint32_t kOffBar = kOffV + kW_StagesV * kKVBytes;
-  // q_full, q_empty, s_full[2], p_full[2], pv_done, mma_done, k_full/empty[SK], v_full/empty[SV]
-  static constexpr int kNumBars = 8 + 2 * kW_StagesK + 2 * kW_StagesV;
+  static constexpr uint32_t kOffRing = kOffQ + kQBytes;
+  static constexpr uint32_t kOffBar = kOffRing + kW_Slots * kKVBytes;
+  // q_full, q_empty, q_tmem, s_full[2], p_full[2], pv_done, mma_done, kv_full[R], kv_empty[R]
+  static constexpr int kNumBars = 9 + 2 * kW_Slots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "dynamic shared memory per block");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;    // buffer b at 64 b; P as 16-bit pairs over its first 32 columns
+  static constexpr uint32_t kColS = 0;    // buffer b at 64 b
+  static constexpr uint32_t kColQ = 128;  // Q as 16-bit pairs, 128 columns
   static constexpr uint32_t kColO = 256;
 };
 
@@ -65,16 +76,13 @@ struct WideBars {
   uint32_t base;
   __device__ uint32_t q_full() const { return base; }
   __device__ uint32_t q_empty() const { return base + 8u; }
-  __device__ uint32_t s_full(int b) const { return base + 16u + 8u * b; }
-  __device__ uint32_t p_full(int b) const { return base + 32u + 8u * b; }
-  __device__ uint32_t pv_done() const { return base + 48u; }
-  __device__ uint32_t mma_done() const { return base + 56u; }
-  __device__ uint32_t k_full(int s) const { return base + 64u + 8u * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 64u + 8u * (kW_StagesK + s); }
-  __device__ uint32_t v_full(int s) const { return base + 64u + 8u * (2 * kW_StagesK + s); }
-  __device__ uint32_t v_empty(int s) const {
-    return base + 64u + 8u * (2 * kW_StagesK + kW_StagesV + s);
-  }
+  __device__ uint32_t q_tmem() const { return base + 16u; }
+  __device__ uint32_t s_full(int b) const { return base + 24u + 8u * b; }
+  __device__ uint32_t p_full(int b) const { return base + 40u + 8u * b; }
+  __device__ uint32_t pv_done() const { return base + 56u; }
+  __device__ uint32_t mma_done() const { return base + 64u; }
+  __device__ uint32_t kv_full(int s) const { return base + 72u + 8u * s; }
+  __device__ uint32_t kv_empty(int s) const { return base + 72u + 8u * (kW_Slots + s); }
 };
 
 struct WideUnit {
@@ -99,12 +107,12 @@ __global__ void __launch_bounds__(kW_Threads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = WideCfg;
-  constexpr int SK = kW_StagesK, SV = kW_StagesV;
+  constexpr int R = kW_Slots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
+  const uint32_t sQ = sbase + C::kOffQ, sRing = sbase + C::kOffRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
   const WideBars bars{sbase + C::kOffBar};
@@ -113,20 +121,17 @@ __global__ void __launch_bounds__(kW_Threads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full(), 1);
-    mbar_init(bars.q_empty(), 1);
+    mbar_init(bars.q_empty(), 4);  // one arrival per softmax warp, after its copy
+    mbar_init(bars.q_tmem(), 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.s_full(b), 1);
       mbar_init(bars.p_full(b), 4);  // one arrival per softmax warp
     }
     mbar_init(bars.pv_done(), 1);
     mbar_init(bars.mma_done(), 1);
-    for (int s = 0; s < SK; ++s) {
-      mbar_init(bars.k_full(s), 1);
-      mbar_init(bars.k_empty(s), 1);
-    }
-    for (int s = 0; s < SV; ++s) {
-      mbar_init(bars.v_full(s), 1);
-      mbar_init(bars.v_empty(s), 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(bars.kv_full(s), 1);
+      mbar_init(bars.kv_empty(s), 1);
     }
     *abort_flag = 0u;
     fence_barrier_init();
@@ -154,7 +159,37 @@ __global__ void __launch_bounds__(kW_Threads, 1)
     uint32_t su[2] = {0u, 0u};  // s_full phases consumed per buffer
     uint32_t pv_seen = 0;       // P.V products issued before the current tile (global count)
     uint32_t gt = 0;            // key tiles processed so far (buffer of tile = gt & 1)
-    bool ok = true;
+    uint32_t qc = 0;            // Q tiles copied into TMEM so far
+    // This row of the staged Q tile into TMEM as 16-bit pairs: 16-byte chunk
+    // c of the row sits in 64-column block c / 8 at row * 128 + ((c % 8) ^
+    // (row % 8)) * 16 (the 128-byte swizzle of the TMA copy).
+    auto copy_q = [&]() -> bool {
+      if (!warp_wait_bar(bars.q_full(), parity_of(qc), wctx)) return false;
+      ++qc;
+#pragma unroll
+      for (int h = 0; h < kW_D / 64; ++h) {
+        uint32_t wv[32];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(
+              smem + C::kOffQ + h * C::kQBlock + row * 128 + ((c8 ^ (row & 7)) << 4));
+          wv[4 * c8] = v4.x;
+          wv[4 * c8 + 1] = v4.y;
+          wv[4 * c8 + 2] = v4.z;
+          wv[4 * c8 + 3] = v4.w;
+        }
+        tmem_st32(tmem + lane_off + C::kColQ + 32 * h, wv);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars.q_empty());  // the staging tile may be refilled
+        mbar_arrive(bars.q_tmem());   // the S MMAs may read Q
+      }
+      return true;
+    };
+    bool ok = unit_index(0) >= p.total_units || copy_q();
     for (int r = 0; ok; ++r) {
       const int idx = unit_index(r);
       if (idx >= p.total_units) break;
@@ -188,29 +223,53 @@ __global__ void __launch_bounds__(kW_Threads, 1)
           for (int i = 0; i < 64; ++i)
             if (i > lim) s[i] = masked;
         }
-        float ev[8];
+        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+        uint32_t pk[32];
+        auto exps = [&](float neg_m) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ev[k] = s[k];
-#pragma unroll
-        for (int i = 8; i < 64; i += 8)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            ev[k] = kNegScale ? fminf(ev[k], s[i + k]) : fmaxf(ev[k], s[i + k]);
-#pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-          for (int k = 0; k < w; ++k)
-            ev[k] = kNegScale ? fminf(ev[k], ev[k + w]) : fmaxf(ev[k], ev[k + w]);
-        const float m_tile = ev[0] * c;
-        const bool rescale = __any_sync(0xffffffffu, m_tile > m_ref + kRescaleThreshold);
+          for (int i = 0; i < 64; i += 4) {
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, s[i], s[i + 1], c, c, neg_m, neg_m);
+            ffma2(x2, x3, s[i + 2], s[i + 3], c, c, neg_m, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            fadd2(sa0, sa1, sa0, sa1, p0, p1);
+            fadd2(sb0, sb1, sb0, sb1, p2, p3);
+            pk[i / 2] = pack_x2<kF16>(p0, p1);
+            pk[i / 2 + 1] = pack_x2<kF16>(p2, p3);
+          }
+        };
+        // Lazy reference, as in the main kernel: P against the current m_ref
+        // with no row extreme; the reference moves to the true maximum only
+        // on the unit's first tile or when the tile's P sum exceeds 2^15.
         // The previous P.V: within the unit, confirmed on this tile; at a
         // unit's first tile it was confirmed by the previous epilogue.
         bool prev_pv_seen = j == 0;
-        if (rescale) {
-          const float m_new = fmaxf(m_ref, m_tile);
+        bool moved = j == 0;
+        if (!moved) {
+          exps(-m_ref);
+          moved = __any_sync(0xffffffffu, !((sa0 + sa1) + (sb0 + sb1) <= kPSumLimit));
+        }
+        if (moved) {
+          float ev[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) ev[k] = s[k];
+#pragma unroll
+          for (int i = 8; i < 64; i += 8)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              ev[k] = kNegScale ? fminf(ev[k], s[i + k]) : fmaxf(ev[k], s[i + k]);
+#pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k)
+              ev[k] = kNegScale ? fminf(ev[k], ev[k + w]) : fmaxf(ev[k], ev[k + w]);
+          const float m_new = fmaxf(m_ref, ev[0] * c);
           const float alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
           l_run *= alpha;
           m_ref = m_new;
+          sa0 = sa1 = sb0 = sb1 = 0.f;
+          exps(-m_ref);
           if (j > 0) {
             // O holds P.V products up to tile j-1 once the last of them is
             // complete (at most one P.V is in flight: the next is issued
@@ -238,21 +297,6 @@ __global__ void __launch_bounds__(kW_Threads, 1)
             }
           }
         }
-        const float neg_m = -m_ref;
-        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          float x0, x1, x2, x3;
-          ffma2(x0, x1, s[i], s[i + 1], c, c, neg_m, neg_m);
-          ffma2(x2, x3, s[i + 2], s[i + 3], c, c, neg_m, neg_m);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          fadd2(sa0, sa1, sa0, sa1, p0, p1);
-          fadd2(sb0, sb1, sb0, sb1, p2, p3);
-          pk[i / 2] = pack_x2<kF16>(p0, p1);
-          pk[i / 2 + 1] = pack_x2<kF16>(p2, p3);
-        }
         tmem_st32(s_addr, pk);
         l_run += (sa0 + sa1) + (sb0 + sb1);
         if (!prev_pv_seen && !warp_wait_bar(bars.pv_done(), parity_of(pv_seen - 1), wctx)) {
@@ -266,29 +310,45 @@ __global__ void __launch_bounds__(kW_Threads, 1)
         ++pv_seen;  // the P.V of this tile is issued after p_full
       }
       if (!ok) break;
+      // The next unit's Q into TMEM: every S MMA of this unit has completed
+      // (the last one was waited for above), so the Q columns are free, and
+      // the next unit's first S MMAs then run during this epilogue.
+      if (unit_index(r + 1) < p.total_units && !copy_q()) break;
       // ------------------------------------------------------------ epilogue
+      // O = O / l in the element type, in two halves of 128 columns (each read
+      // from TMEM with one wait), straight to global memory: each thread
+      // writes its own row, 32-byte stores where O's alignment allows.
       if (!warp_wait_bar(bars.pv_done(), parity_of(pv_seen - 1), wctx)) break;
       tc_fence_after_sync();
       const float inv_l = 1.0f / l_run;
       const bool in_range = q_idx < p.N;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + u.b * p.o_sb + u.h * p.o_sh + q_idx * p.o_sn);
+      uint16_t* orow = p.o + u.b * p.o_sb + u.h * p.o_sh + q_idx * p.o_sn;
 #pragma unroll 1
-      for (int cc = 0; cc < kW_D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + 32 * cc, o);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t ov[128];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          tmem_ld32(o_addr + 128 * hh + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&ov[32 * cc]));
         tmem_ld_wait();
-        tmem_ld_fence(o);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t w4[4];
+        for (int cc = 0; cc < 4; ++cc) tmem_ld_fence(*reinterpret_cast<uint32_t(*)[32]>(&ov[32 * cc]));
+        uint32_t w[64];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float a0, a1;
-            fmul2(a0, a1, __uint_as_float(o[8 * g + 2 * e]), __uint_as_float(o[8 * g + 2 * e + 1]),
-                  inv_l, inv_l);
-            w4[e] = pack_x2<kF16>(a0, a1);
+        for (int i = 0; i < 64; ++i) {
+          float a0, a1;
+          fmul2(a0, a1, __uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1]), inv_l, inv_l);
+          w[i] = pack_x2<kF16>(a0, a1);
+        }
+        if (in_range) {
+          if (p.o_vec32) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) st_global_v8(orow + 128 * hh + 16 * g, &w[8 * g]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 128 * hh);
+#pragma unroll
+            for (int g = 0; g < 16; ++g)
+              dst[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
           }
-          if (in_range) dst[4 * cc + g] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
       if (in_range)
@@ -298,74 +358,53 @@ __global__ void __launch_bounds__(kW_Threads, 1)
       tc_fence_before_sync();
     }
   } else if (warp == kW_LoadWarp) {
-    // ------------------------------------------------------------ Q, K producer
+    // ------------------------------------------------------------ Q, K, V producer
     if (lane == 0) {
       const uint64_t keep = make_l2_policy_evict_last();
       const uint64_t once = make_l2_policy_evict_first();
-      uint32_t kc = 0, qc = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
+      uint32_t ic = 0, qc = 0;  // K/V items and Q tiles issued so far
+      int cur_h = 0, cur_b = 0;
+      // One K or V tile into the next ring slot, once that slot is free.
+      auto issue = [&](const CUtensorMap* map, int row0) -> bool {
+        const int s = static_cast<int>(ic % R);
+        if (ic >= static_cast<uint32_t>(R) &&
+            !wait_bar(bars.kv_empty(s), parity_of(ic / R - 1), wctx))
+          return false;
+        mbar_arrive_expect_tx(bars.kv_full(s), C::kKVBytes);
+#pragma unroll
+        for (int b = 0; b < kW_D / 64; ++b)
+          tma_load_4d_hint(sRing + s * C::kKVBytes + b * C::kKVBlock, map, bars.kv_full(s), 64 * b,
+                           row0, cur_h, cur_b, keep);
+        ++ic;
+        return true;
+      };
+      for (int r = 0;; ++r) {
         const int idx = unit_index(r);
         if (idx >= p.total_units) break;
         const WideUnit u = wide_unit_at(idx, p);
+        cur_h = u.h;
+        cur_b = u.b;
+        // Q of this unit replaces the previous one in the staging tile once
+        // the softmax warps have copied that one into TMEM (q_empty).
         if (qc > 0 && !wait_bar(bars.q_empty(), parity_of(qc - 1), wctx)) break;
         mbar_arrive_expect_tx(bars.q_full(), C::kQBytes);
 #pragma unroll
         for (int b = 0; b < kW_D / 64; ++b)
           tma_load_4d_hint(sQ + b * C::kQBlock, &tm_q, bars.q_full(), 64 * b, u.q0, u.h, u.b, once);
         ++qc;
-        for (int j = 0; j < u.n; ++j) {
-          const int s = static_cast<int>(kc % SK);
-          if (kc >= static_cast<uint32_t>(SK) &&
-              !wait_bar(bars.k_empty(s), parity_of(kc / SK - 1), wctx)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bars.k_full(s), C::kKVBytes);
-#pragma unroll
-          for (int b = 0; b < kW_D / 64; ++b)
-            tma_load_4d_hint(sK + s * C::kKVBytes + b * C::kKVBlock, &tm_k, bars.k_full(s), 64 * b,
-                             j * kW_BlockN, u.h, u.b, keep);
-          ++kc;
-        }
+        // Items in the order the MMAs read them: K_0, K_1, then V_j, K_j+2.
+        bool ok = issue(&tm_k, 0) && (u.n < 2 || issue(&tm_k, kW_BlockN));
+        for (int j = 0; ok && j < u.n; ++j)
+          ok = issue(&tm_v, j * kW_BlockN) && (j + 2 >= u.n || issue(&tm_k, (j + 2) * kW_BlockN));
+        if (!ok) break;
       }
+      // Drain: every copy issued must land before the CTA may exit.  The last
+      // item in slot s is the largest count < ic congruent to s mod R.
       if (qc > 0) wait_bar_drain(bars.q_full(), parity_of(qc - 1), wctx);
-      for (int s = 0; s < SK; ++s) {
-        if (kc > static_cast<uint32_t>(s)) {
-          const uint32_t last = kc - 1 - ((kc - 1 - s) % SK);
-          wait_bar_drain(bars.k_full(s), parity_of(last / SK), wctx);
-        }
-      }
-    }
-  } else if (warp == kW_LoadVWarp) {
-    // ------------------------------------------------------------ V producer
-    if (lane == 0) {
-      const uint64_t keep = make_l2_policy_evict_last();
-      uint32_t vc = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int idx = unit_index(r);
-        if (idx >= p.total_units) break;
-        const WideUnit u = wide_unit_at(idx, p);
-        for (int j = 0; j < u.n; ++j) {
-          const int s = static_cast<int>(vc % SV);
-          if (vc >= static_cast<uint32_t>(SV) &&
-              !wait_bar(bars.v_empty(s), parity_of(vc / SV - 1), wctx)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bars.v_full(s), C::kKVBytes);
-#pragma unroll
-          for (int b = 0; b < kW_D / 64; ++b)
-            tma_load_4d_hint(sV + s * C::kKVBytes + b * C::kKVBlock, &tm_v, bars.v_full(s), 64 * b,
-                             j * kW_BlockN, u.h, u.b, keep);
-          ++vc;
-        }
-      }
-      for (int s = 0; s < SV; ++s) {
-        if (vc > static_cast<uint32_t>(s)) {
-          const uint32_t last = vc - 1 - ((vc - 1 - s) % SV);
-          wait_bar_drain(bars.v_full(s), parity_of(last / SV), wctx);
+      for (int s = 0; s < R; ++s) {
+        if (ic > static_cast<uint32_t>(s)) {
+          const uint32_t last = ic - 1 - ((ic - 1 - s) % R);
+          wait_bar_drain(bars.kv_full(s), parity_of(last / R), wctx);
         }
       }
     }
@@ -377,27 +416,27 @@ __global__ void __launch_bounds__(kW_Threads, 1)
                                       : idesc_bf16_f32(kW_TileM, kW_BlockN, 0, 0);
     constexpr uint32_t kIdescPV = kF16 ? idesc_f16_f32(kW_TileM, kW_D, 0, 1)
                                        : idesc_bf16_f32(kW_TileM, kW_D, 0, 1);
-    const uint32_t q_lo = desc_lo(sQ, 16);
-    const uint32_t k_lo = desc_lo(sK, 16);
-    const uint32_t v_lo = desc_lo(sV, C::kKVBlock);  // MN-major: 64-column blocks 8 KB apart
+    const uint32_t k_lo = desc_lo(sRing, 16);             // K slots, K-major
+    const uint32_t v_lo = desc_lo(sRing, C::kKVBlock);    // V slots, MN-major: 64-column blocks 8 KB apart
     auto commit = [&](uint32_t bar) {
       if (leader) umma_commit(bar);
       __syncwarp();
     };
-    auto issue_s = [&](int b, uint32_t k_stage) {  // S_b = Q K^T, 16 K-slices of 16 columns
-      const uint32_t kb = k_lo + ((k_stage * C::kKVBytes) >> 4);
+    // S_b = Q K^T: Q (16-bit pairs) from TMEM, 16 K-slices of 16 columns of
+    // the K tile in ring slot `slot`.
+    auto issue_s = [&](int b, uint32_t slot) {
+      const uint32_t kb = k_lo + ((slot * C::kKVBytes) >> 4);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kW_D / 16; ++kk)
-          umma_ss_lohi(tmem + C::kColS + 64u * b,
-                       q_lo + (((kk >> 2) * C::kQBlock + (kk & 3) * 32) >> 4), kHi,
+          umma_ts_lohi(tmem + C::kColS + 64u * b, tmem + C::kColQ + 8u * kk,
                        kb + (((kk >> 2) * C::kKVBlock + (kk & 3) * 32) >> 4), kHi, kIdescS,
                        kk > 0 ? 1u : 0u);
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int b, uint32_t v_stage, bool first) {  // O (+)= P_b V, 4 slices of 16 keys
-      const uint32_t vb = v_lo + ((v_stage * C::kKVBytes) >> 4);
+    auto issue_pv = [&](int b, uint32_t slot, bool first) {  // O (+)= P_b V, 4 slices of 16 keys
+      const uint32_t vb = v_lo + ((slot * C::kKVBytes) >> 4);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kW_BlockN / 16; ++kk)
@@ -406,53 +445,52 @@ __global__ void __launch_bounds__(kW_Threads, 1)
       }
       __syncwarp();
     };
-    uint32_t kc = 0, vc = 0, qc = 0, gt = 0;
-    uint32_t pu[2] = {0u, 0u};  // p_full phases consumed per buffer
+    uint32_t ic = 0, qt = 0, gt = 0;  // ring items consumed, Q copies consumed, key tiles
+    uint32_t pu[2] = {0u, 0u};        // p_full phases consumed per buffer
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int idx = unit_index(r);
       if (idx >= p.total_units) break;
       const WideUnit u = wide_unit_at(idx, p);
-      if (!warp_wait_bar(bars.q_full(), parity_of(qc), wctx)) break;
-      ++qc;
+      if (!warp_wait_bar(bars.q_tmem(), parity_of(qt), wctx)) break;
+      ++qt;
+      tc_fence_after_sync();
       // S(0) and S(1) ahead of the softmax.
       for (int j = 0; ok && j < 2 && j < u.n; ++j) {
-        if (!warp_wait_bar(bars.k_full(kc % SK), parity_of(kc / SK), wctx)) {
+        if (!warp_wait_bar(bars.kv_full(ic % R), parity_of(ic / R), wctx)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        issue_s(static_cast<int>((gt + j) & 1u), kc % SK);
+        issue_s(static_cast<int>((gt + j) & 1u), ic % R);
         commit(bars.s_full(static_cast<int>((gt + j) & 1u)));
-        commit(bars.k_empty(kc % SK));
-        if (j == u.n - 1) commit(bars.q_empty());  // last S of the unit
-        ++kc;
+        commit(bars.kv_empty(ic % R));
+        ++ic;
       }
       for (int j = 0; ok && j < u.n; ++j) {
         const int b = static_cast<int>((gt + j) & 1u);
-        if (!warp_wait_bar(bars.v_full(vc % SV), parity_of(vc / SV), wctx) ||
+        if (!warp_wait_bar(bars.kv_full(ic % R), parity_of(ic / R), wctx) ||
             !warp_wait_bar(bars.p_full(b), parity_of(pu[b]), wctx)) {
           ok = false;
           break;
         }
         ++pu[b];
         tc_fence_after_sync();
-        issue_pv(b, vc % SV, j == 0);
-        commit(bars.v_empty(vc % SV));
+        issue_pv(b, ic % R, j == 0);
+        commit(bars.kv_empty(ic % R));
         commit(bars.pv_done());
-        ++vc;
+        ++ic;
         if (j + 2 < u.n) {
           // S(j+2) overwrites P(j) in buffer b after the P.V that reads it.
-          if (!warp_wait_bar(bars.k_full(kc % SK), parity_of(kc / SK), wctx)) {
+          if (!warp_wait_bar(bars.kv_full(ic % R), parity_of(ic / R), wctx)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          issue_s(b, kc % SK);
+          issue_s(b, ic % R);
           commit(bars.s_full(b));
-          commit(bars.k_empty(kc % SK));
-          if (j + 2 == u.n - 1) commit(bars.q_empty());
-          ++kc;
+          commit(bars.kv_empty(ic % R));
+          ++ic;
         }
       }
       gt += static_cast<uint32_t>(u.n);
