@@ -58,7 +58,7 @@ NCU_TRAFFIC_BYTES_DECODE = {
 # out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
     "b2h16n4096d128_causal": 140_705_280,
-    "b2h16n4096d256_causal": 571_343_616,
+    "b2h16n4096d256_causal": 579_028_224,
 }
 
 
