@@ -46,6 +46,14 @@ DECODE_UNIT = "GB/s"
 BWD_METRIC = "attention bwd TFLOPS (nominal 2.5x forward FLOPs) & % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+# NVIDIA's published dense (no 2:4 sparsity) BF16/FP16 tensor rate of one
+# Blackwell Ultra (GB300) GPU, reported beside the measured peak.
+NOMINAL_BF16_TFLOPS = 2250.0
+# exp2 (MUFU) throughput per SM per clock, measured on GB300 with a
+# microbenchmark of back-to-back ex2.approx.ftz.f32: the forward's secondary
+# ceiling (one exponential per visible score).
+EX2_PER_CLK_PER_SM = 32
+NUM_SMS = 152
 # DRAM bytes (read + write) of one split-KV call (the clustered split pass),
 # from one ncu capture per workload (profiles/); a workload is left out
 # until a capture of the kernel as benchmarked exists.
@@ -459,14 +467,27 @@ def run_ours(args, w):
             what = ("the whole workload (every row of every head)" if n_rows == w.N else
                     f"{n_rows} seeded query rows per head x {w.B * w.H} heads "
                     f"({100.0 * n_rows / w.N:.2f}% of the rows)")
+            full_exact = 4.0 * w.d * w.B * w.H * (w.N * (w.N + 1) / 2 if w.causal else w.N * w.N)
             cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-                   "sample": f"{what}, {reps} time(s), fp64 oracle, {dt:.1f} s"}
+                   "sample": f"{what}, {reps} time(s), fp64 oracle, {dt:.1f} s",
+                   "extrapolated_full_s": dt * full_exact / fl,
+                   "extrapolation": "time of the whole workload at the sample's FLOP rate "
+                                    "(an extrapolation, not a measurement)"}
+        # One exponential per visible score element (the exact causal count).
+        n_exp = w.B * w.H * (w.N * (w.N + 1) / 2 if w.causal else w.N * w.N)
+        sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        ex2_peak = EX2_PER_CLK_PER_SM * NUM_SMS * sm_mhz * 1e6 / 1e9
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
                         "; fp16 x 1: its nominal dense rate equals bf16's"
                         if elem == "f16" else ""),
-                    "traffic": None if args.loop_order else NCU_TRAFFIC_BYTES.get(w.name)}
+                    "traffic": None if args.loop_order else NCU_TRAFFIC_BYTES.get(w.name),
+                    "secondary": {"what": "exp2 (MUFU) rate, one per visible score",
+                                  "achieved": n_exp / avg_launch_s / 1e9, "peak": ex2_peak,
+                                  "unit": "Gexp/s", "frac": n_exp / avg_launch_s / 1e9 / ex2_peak,
+                                  "peak_source": f"{EX2_PER_CLK_PER_SM}/clk/SM measured x "
+                                                 f"{NUM_SMS} SMs x {sm_mhz:.0f} MHz"}}
         if args.loop_order == 1:
             # The K/V-outer order moves the running state through HBM every
             # step: its own algorithmic bytes bound it.
@@ -489,6 +510,10 @@ def run_ours(args, w):
                            "kernel": "fa_fwd_order_ablation (64x64 tiles, warp MMAs)"}
                           if args.loop_order else {})},
             "pct_of_peak": 100.0 * achieved / peak,
+            "pct_of_nominal": 100.0 * achieved / NOMINAL_BF16_TFLOPS,
+            "nominal_peak": {"value": NOMINAL_BF16_TFLOPS, "unit": "TFLOP/s",
+                             "source": "NVIDIA Blackwell Ultra (GB300) dense BF16 tensor rate "
+                                       "per GPU, without 2:4 sparsity"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
