@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -386,14 +387,16 @@ int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensor
                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                const CUtensorMap& mq64, const CUtensorMap& mk64, const CUtensorMap& mv64,
                const CUtensorMap& mdo64, const fa::BwdParams& base, const fa::BwdParams& prm_q,
-               cudaStream_t stream) {
+               int sms, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(base.num_bh) * base.Npad;
   const int64_t threads = rows * (D / 8);  // a multiple of 256: Npad is a multiple of 128
   fa::fa_bwd_prep_kernel<D><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
       const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  const unsigned ctas = static_cast<unsigned>(static_cast<int64_t>(base.T) * base.num_bh);
+  // Persistent grids: one CTA per SM (at most one per tile) walks the tiles.
+  const unsigned ctas = static_cast<unsigned>(
+      std::min<int64_t>(static_cast<int64_t>(base.T) * base.num_bh, sms));
   fa::fa_bwd_kernel<D, true><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, true>::kSmemAlloc, stream>>>(
       mk, mv, mq64, mdo64, base);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
@@ -476,9 +479,9 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   prm_q.out1 = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return d == 64 ? launch_bwd<64>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
-                                  prm_q, st)
+                                  prm_q, sms, st)
                  : launch_bwd<128>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
-                                   prm_q, st);
+                                   prm_q, sms, st);
 }
 
 // ------------------------------------------------------- loop-order ablation

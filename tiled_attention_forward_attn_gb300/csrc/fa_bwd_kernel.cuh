@@ -101,9 +101,9 @@ struct BwdCfg {
   static constexpr uint32_t kOffY = 2 * kTileBytes;   // ring of (Y0, Y1) halves
   static constexpr uint32_t kOffVec = kOffY + kStages * kStageBytes;
   static constexpr uint32_t kOffBar = kOffVec + kStages * kVecBytes;
-  // x_full, st_full[2], p_full[2], acc_done, y_full[S], y_empty[S]
-  // ... and x_tmem (query-tile pass: X copied into TMEM)
-  static constexpr int kNumBars = 7 + 2 * kStages;
+  // x_full, st_full[2], p_full[2], acc_done, y_full[S], y_empty[S], x_tmem
+  // (query-tile pass: X copied into TMEM), x_empty, acc_free, mma_done
+  static constexpr int kNumBars = 10 + 2 * kStages;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -129,6 +129,12 @@ struct BwdBars {
   __device__ uint32_t y_full(int s) const { return base + 48u + 8u * s; }
   __device__ uint32_t y_empty(int s) const { return base + 48u + 8u * (stages + s); }
   __device__ uint32_t x_tmem() const { return base + 48u + 16u * stages; }
+  // The stationary tile's shared memory may be refilled (key-tile pass: its
+  // last S/dP MMAs are complete; query-tile pass: it is copied into TMEM).
+  __device__ uint32_t x_empty() const { return base + 56u + 16u * stages; }
+  // The accumulators of a tile have been read by its epilogue.
+  __device__ uint32_t acc_free() const { return base + 64u + 16u * stages; }
+  __device__ uint32_t mma_done() const { return base + 72u + 16u * stages; }
 };
 
 // -D_i = -rowsum(dO_i * O_i) and -LSE_i * log2(e) for every row of the
@@ -187,14 +193,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Tile of this CTA, heaviest first under the causal mask: key tile 0 meets
-  // every query tile; query tile T-1 meets every key tile.
-  const int band = static_cast<int>(blockIdx.x) / p.num_bh;
-  const int bh = static_cast<int>(blockIdx.x) - band * p.num_bh;
-  const int xt = kKV ? band : p.T - 1 - band;
-  const int y_first = (kKV && p.causal) ? xt : 0;
-  const int y_last = (!kKV && p.causal) ? xt : p.T - 1;
-  const int steps = y_last - y_first + 1;
+  // The grid is persistent: CTA c takes the tiles unit_index(0), (1), ...
+  // of the order below, dealt in a serpentine like the forward's units.
+  // Tile t, heaviest first under the causal mask: key tile 0 meets every
+  // query tile; query tile T-1 meets every key tile.
+  struct Tile {
+    int bh, xt, y_first, steps;
+  };
+  const int total = p.num_bh * p.T;
+  auto tile_at = [&](int t) -> Tile {
+    const int band = t / p.num_bh;
+    Tile u;
+    u.bh = t - band * p.num_bh;
+    u.xt = kKV ? band : p.T - 1 - band;
+    u.y_first = (kKV && p.causal) ? u.xt : 0;
+    const int y_last = (!kKV && p.causal) ? u.xt : p.T - 1;
+    u.steps = y_last - u.y_first + 1;
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bars.x_full(), 1);
@@ -204,6 +220,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bars.acc_done(), 1);
     mbar_init(bars.x_tmem(), 4 * kBwdEwGroups);  // one arrival per elementwise warp
+    // Key-tile pass: a commit after a tile's last S/dP MMAs; query-tile
+    // pass: one arrival per elementwise warp after the copy into TMEM.
+    mbar_init(bars.x_empty(), kKV ? 1 : 4 * kBwdEwGroups);
+    mbar_init(bars.acc_free(), 4 * kBwdEwGroups);
+    mbar_init(bars.mma_done(), 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.y_full(s), 1);
       mbar_init(bars.y_empty(s), 1);
@@ -238,121 +259,143 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int g = warp >> 2;            // warpgroup: its 16 columns of every sub-step
     const int row = threadIdx.x & 127;  // = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
     const float cs = p.scale_log2;
-    if (!kKV) {
-      // Warpgroups 0 and 1 copy this row of X_g (g = 0: Q_i, 1: dO_i) from the swizzled SMEM
-      // tile into TMEM as bf16 pairs: 16-byte chunk c of the row sits in
-      // 64-column block c / 8 at row * 128 + ((c % 8) ^ (row % 8)) * 16.
-      bool got = g < 2 && warp_wait_bar(bars.x_full(), 0, wctx);
-      if (got) {
-        const uint8_t* xt_s = smem + C::kOffX + g * C::kTileBytes;
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          uint32_t wv[32];
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint4 v4 = *reinterpret_cast<const uint4*>(
-                xt_s + h * kSwBlockBytes + row * 128 + (((c8 ^ (row & 7))) << 4));
-            wv[4 * c8] = v4.x;
-            wv[4 * c8 + 1] = v4.y;
-            wv[4 * c8 + 2] = v4.z;
-            wv[4 * c8 + 3] = v4.w;
+    uint32_t gsub = 0;  // sub-steps of earlier tiles (always even)
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int t = unit_index(r);
+      if (t >= total) break;
+      const Tile u = tile_at(t);
+      const int bh = u.bh, xt = u.xt, y_first = u.y_first, steps = u.steps;
+      const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
+      if (!kKV) {
+        // Warpgroups 0 and 1 copy this row of X_g (g = 0: Q_i, 1: dO_i) from the swizzled SMEM
+        // tile into TMEM as bf16 pairs: 16-byte chunk c of the row sits in
+        // 64-column block c / 8 at row * 128 + ((c % 8) ^ (row % 8)) * 16.  The
+        // previous tile's S/dP MMAs, the only readers of these columns, are
+        // complete: its last st_full was consumed.
+        if (g < 2) {
+          if (!warp_wait_bar(bars.x_full(), parity_of(r), wctx)) {
+            ok = false;
+            break;
           }
-          tmem_st32(tmem + lane_off + C::kColXT + g * (D / 2) + 32 * h, wv);
+          const uint8_t* xt_s = smem + C::kOffX + g * C::kTileBytes;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            uint32_t wv[32];
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              const uint4 v4 = *reinterpret_cast<const uint4*>(
+                  xt_s + h * kSwBlockBytes + row * 128 + (((c8 ^ (row & 7))) << 4));
+              wv[4 * c8] = v4.x;
+              wv[4 * c8 + 1] = v4.y;
+              wv[4 * c8 + 2] = v4.z;
+              wv[4 * c8 + 3] = v4.w;
+            }
+            tmem_st32(tmem + lane_off + C::kColXT + g * (D / 2) + 32 * h, wv);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bars.x_tmem());
+          mbar_arrive(bars.x_empty());
+        }
+      }
+      float nlse_r = 0.0f, nd_r = 0.0f;
+      if (!kKV) {
+        nlse_r = p.lse2[static_cast<size_t>(bh) * p.Npad + x_idx];
+        nd_r = p.dvec[static_cast<size_t>(bh) * p.Npad + x_idx];
+      }
+      for (int m = 0; m < 2 * steps; ++m) {
+        const int b = m & 1;  // TMEM buffer
+        const int n = m >> 1;
+        const uint32_t gm = gsub + static_cast<uint32_t>(m);  // sub-step over all tiles
+        if (!warp_wait_bar(bars.st_full(b), parity_of(gm >> 1), wctx)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const int yt = y_first + n;
+        const int y0 = yt * kBwdTile + kBwdSub * b + kBwdEwCols * g;  // first streamed row here
+        const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdEwCols > p.N);
+        const float4* vec = reinterpret_cast<const float4*>(smem + C::kOffVec + (gm % S) * C::kVecBytes) +
+                            (kBwdEwCols / 4) * g;
+        const uint32_t col_s = C::kColS + kBwdSub * b + kBwdEwCols * g;
+        const uint32_t col_dp = C::kColDP + kBwdSub * b + kBwdEwCols * g;
+        uint32_t sr[kBwdEwCols], dr[kBwdEwCols];
+        tmem_ld16(tmem + lane_off + col_s, sr);
+        tmem_ld16(tmem + lane_off + col_dp, dr);
+        tmem_ld_wait();
+        tmem_ld_fence16(sr);
+        tmem_ld_fence16(dr);
+        uint32_t pp[kBwdEwCols / 2], pd[kBwdEwCols / 2];
+#pragma unroll
+        for (int e = 0; e < kBwdEwCols; e += 4) {
+          // -LSE2 and -D of the four columns (kKV: per column, from shared
+          // memory; otherwise this row's).
+          float nl[4], nd[4];
+          if (kKV) {
+            const float4 a = vec[e / 4];
+            const float4 c4 = vec[(kBwdSub + e) / 4];
+            nl[0] = a.x; nl[1] = a.y; nl[2] = a.z; nl[3] = a.w;
+            nd[0] = c4.x; nd[1] = c4.y; nd[2] = c4.z; nd[3] = c4.w;
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              nl[h] = nlse_r;
+              nd[h] = nd_r;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 4; h += 2) {
+            float x0, x1, p0, p1, t0, t1, d0, d1;
+            ffma2(x0, x1, __uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1]), cs, cs, nl[h],
+                  nl[h + 1]);
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+            if (need_mask) {
+              // key <= query when causal; padding rows past N see nothing.
+              const int ya = y0 + e + h;
+              const bool va = ya < p.N && (!p.causal || (kKV ? x_idx <= ya : ya <= x_idx));
+              const bool vb = ya + 1 < p.N &&
+                              (!p.causal || (kKV ? x_idx <= ya + 1 : ya + 1 <= x_idx));
+              if (!va) p0 = 0.0f;
+              if (!vb) p1 = 0.0f;
+            }
+            fadd2(t0, t1, __uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1]), nd[h],
+                  nd[h + 1]);
+            fmul2(d0, d1, p0, p1, t0, t1);
+            pp[(e + h) / 2] = pack_bf16x2(p0, p1);
+            pd[(e + h) / 2] = pack_bf16x2(d0, d1);
+          }
+        }
+        // The pairs go into the first 8 of this warpgroup's 16 columns, which
+        // it has already read: the A operand of accumulation slice g.
+        if (kKV) {
+          tmem_st8(tmem + lane_off + col_s, pp);
+          tmem_st8(tmem + lane_off + col_dp, pd);
+        } else {
+          tmem_st8(tmem + lane_off + col_s, pd);
         }
         tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.p_full(b));
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.x_tmem());
-    }
-    float nlse_r = 0.0f, nd_r = 0.0f;
-    if (!kKV) {
-      nlse_r = p.lse2[static_cast<size_t>(bh) * p.Npad + x_idx];
-      nd_r = p.dvec[static_cast<size_t>(bh) * p.Npad + x_idx];
-    }
-    bool ok = true;
-    for (int m = 0; m < 2 * steps; ++m) {
-      const int b = m & 1;  // TMEM buffer
-      const int n = m >> 1;
-      if (!warp_wait_bar(bars.st_full(b), parity_of(n), wctx)) {
+      if (!ok) break;
+      gsub += static_cast<uint32_t>(2 * steps);
+      // -------------------------------------------------------------- epilogue
+      // kKV: warpgroups 0 and 1 store the two column halves of dK (scaled), 2
+      // and 3 those of dV; otherwise each warpgroup stores a quarter of dQ's
+      // columns (scaled).  The accumulators are read with one wait and
+      // released (acc_free) before the stores, so the next tile's first
+      // accumulation does not wait for them.
+      if (!warp_wait_bar(bars.acc_done(), parity_of(r), wctx)) {
         ok = false;
         break;
       }
-      tc_fence_after_sync();
-      const int yt = y_first + n;
-      const int y0 = yt * kBwdTile + kBwdSub * b + kBwdEwCols * g;  // first streamed row here
-      const bool need_mask = (p.causal && yt == xt) || (y0 + kBwdEwCols > p.N);
-      const float4* vec = reinterpret_cast<const float4*>(smem + C::kOffVec + (m % S) * C::kVecBytes) +
-                          (kBwdEwCols / 4) * g;
-      const uint32_t col_s = C::kColS + kBwdSub * b + kBwdEwCols * g;
-      const uint32_t col_dp = C::kColDP + kBwdSub * b + kBwdEwCols * g;
-      uint32_t sr[kBwdEwCols], dr[kBwdEwCols];
-      tmem_ld16(tmem + lane_off + col_s, sr);
-      tmem_ld16(tmem + lane_off + col_dp, dr);
-      tmem_ld_wait();
-      tmem_ld_fence16(sr);
-      tmem_ld_fence16(dr);
-      uint32_t pp[kBwdEwCols / 2], pd[kBwdEwCols / 2];
-#pragma unroll
-      for (int e = 0; e < kBwdEwCols; e += 4) {
-        // -LSE2 and -D of the four columns (kKV: per column, from shared
-        // memory; otherwise this row's).
-        float nl[4], nd[4];
-        if (kKV) {
-          const float4 a = vec[e / 4];
-          const float4 c4 = vec[(kBwdSub + e) / 4];
-          nl[0] = a.x; nl[1] = a.y; nl[2] = a.z; nl[3] = a.w;
-          nd[0] = c4.x; nd[1] = c4.y; nd[2] = c4.z; nd[3] = c4.w;
-        } else {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            nl[h] = nlse_r;
-            nd[h] = nd_r;
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < 4; h += 2) {
-          float x0, x1, p0, p1, t0, t1, d0, d1;
-          ffma2(x0, x1, __uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1]), cs, cs, nl[h],
-                nl[h + 1]);
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
-          if (need_mask) {
-            // key <= query when causal; padding rows past N see nothing.
-            const int ya = y0 + e + h;
-            const bool va = ya < p.N && (!p.causal || (kKV ? x_idx <= ya : ya <= x_idx));
-            const bool vb = ya + 1 < p.N &&
-                            (!p.causal || (kKV ? x_idx <= ya + 1 : ya + 1 <= x_idx));
-            if (!va) p0 = 0.0f;
-            if (!vb) p1 = 0.0f;
-          }
-          fadd2(t0, t1, __uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1]), nd[h],
-                nd[h + 1]);
-          fmul2(d0, d1, p0, p1, t0, t1);
-          pp[(e + h) / 2] = pack_bf16x2(p0, p1);
-          pd[(e + h) / 2] = pack_bf16x2(d0, d1);
-        }
-      }
-      // The pairs go into the first 8 of this warpgroup's 16 columns, which
-      // it has already read: the A operand of accumulation slice g.
-      if (kKV) {
-        tmem_st8(tmem + lane_off + col_s, pp);
-        tmem_st8(tmem + lane_off + col_dp, pd);
-      } else {
-        tmem_st8(tmem + lane_off + col_s, pd);
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.p_full(b));
-    }
-    // ---------------------------------------------------------------- epilogue
-    // kKV: warpgroups 0 and 1 store the two column halves of dK (scaled), 2
-    // and 3 those of dV; otherwise each warpgroup stores a quarter of dQ's
-    // columns (scaled).
-    if (ok && warp_wait_bar(bars.acc_done(), 0, wctx)) {
       tc_fence_after_sync();
       const bool in_range = x_idx < p.N;
       constexpr int kCols = kKV ? D / 2 : D / 4;
@@ -363,21 +406,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint16_t* out = is_dv ? p.out1 : p.out0;
       uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * D +
                                             kCols * part);
+      uint32_t racc[kCols];
 #pragma unroll
-      for (int cc = 0; cc < kCols / 16; ++cc) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_off + col + 16 * cc, r);
-        tmem_ld_wait();
-        tmem_ld_fence16(r);
+      for (int cc = 0; cc < kCols / 16; ++cc)
+        tmem_ld16(tmem + lane_off + col + 16 * cc, *reinterpret_cast<uint32_t(*)[16]>(&racc[16 * cc]));
+      tmem_ld_wait();
 #pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          uint32_t w4[4];
+      for (int cc = 0; cc < kCols / 16; ++cc)
+        tmem_ld_fence16(*reinterpret_cast<uint32_t(*)[16]>(&racc[16 * cc]));
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.acc_free());
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w4[e] = pack_bf16x2(__uint_as_float(r[8 * q4 + 2 * e]) * mul,
-                                __uint_as_float(r[8 * q4 + 2 * e + 1]) * mul);
-          if (in_range) dst[2 * cc + q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
+      for (int q8 = 0; q8 < kCols / 8; ++q8) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w4[e] = pack_bf16x2(__uint_as_float(racc[8 * q8 + 2 * e]) * mul,
+                              __uint_as_float(racc[8 * q8 + 2 * e + 1]) * mul);
+        if (in_range) dst[q8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
     }
   } else if (warp == kBwdLoadWarp) {
@@ -386,40 +433,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Y tiles are read by every X tile of the same head: keep them in L2.
       const uint64_t keep = make_l2_policy_evict_last();
       const uint64_t once = make_l2_policy_evict_first();
-      mbar_arrive_expect_tx(bars.x_full(), 2 * C::kTileBytes);
-#pragma unroll
-      for (int b = 0; b < D / 64; ++b) {
-        tma_load_3d_hint(sX + b * kSwBlockBytes, &tm_x0, bars.x_full(), 64 * b, xt * kBwdTile, bh,
-                         once);
-        tma_load_3d_hint(sX + C::kTileBytes + b * kSwBlockBytes, &tm_x1, bars.x_full(), 64 * b,
-                         xt * kBwdTile, bh, once);
-      }
-      int issued = 0;
-      for (int m = 0; m < 2 * steps; ++m) {
-        const int s = m % S;
-        if (m >= S && !wait_bar(bars.y_empty(s), parity_of(m / S - 1), wctx)) break;
-        const int row0 = (y_first + (m >> 1)) * kBwdTile + kBwdSub * (m & 1);
-        const uint32_t stage = sY + s * C::kStageBytes;
-        mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes + C::kVecBytes);
+      uint32_t yc = 0;  // Y stages issued over all tiles
+      int nx = 0;       // X tiles issued
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int t = unit_index(r);
+        if (t >= total) break;
+        const Tile u = tile_at(t);
+        // X of this tile replaces the previous one once that one is no longer
+        // read from shared memory (x_empty).
+        if (r > 0 && !wait_bar(bars.x_empty(), parity_of(r - 1), wctx)) break;
+        mbar_arrive_expect_tx(bars.x_full(), 2 * C::kTileBytes);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_3d_hint(stage + b * C::kHalfBlock, &tm_y0, bars.y_full(s), 64 * b, row0, bh, keep);
-          tma_load_3d_hint(stage + C::kHalfBytes + b * C::kHalfBlock, &tm_y1, bars.y_full(s),
-                           64 * b, row0, bh, keep);
+          tma_load_3d_hint(sX + b * kSwBlockBytes, &tm_x0, bars.x_full(), 64 * b,
+                           u.xt * kBwdTile, u.bh, once);
+          tma_load_3d_hint(sX + C::kTileBytes + b * kSwBlockBytes, &tm_x1, bars.x_full(), 64 * b,
+                           u.xt * kBwdTile, u.bh, once);
         }
-        if (kKV) {
-          const size_t v0 = static_cast<size_t>(bh) * p.Npad + row0;
-          const uint32_t vec = sbase + C::kOffVec + s * C::kVecBytes;
-          bulk_load(vec, p.lse2 + v0, kBwdSub * 4, bars.y_full(s));
-          bulk_load(vec + kBwdSub * 4, p.dvec + v0, kBwdSub * 4, bars.y_full(s));
+        ++nx;
+        for (int m = 0; m < 2 * u.steps; ++m, ++yc) {
+          const int s = static_cast<int>(yc % S);
+          if (yc >= static_cast<uint32_t>(S) &&
+              !wait_bar(bars.y_empty(s), parity_of(yc / S - 1), wctx)) {
+            ok = false;
+            break;
+          }
+          const int row0 = (u.y_first + (m >> 1)) * kBwdTile + kBwdSub * (m & 1);
+          const uint32_t stage = sY + s * C::kStageBytes;
+          mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes + C::kVecBytes);
+#pragma unroll
+          for (int b = 0; b < D / 64; ++b) {
+            tma_load_3d_hint(stage + b * C::kHalfBlock, &tm_y0, bars.y_full(s), 64 * b, row0, u.bh,
+                             keep);
+            tma_load_3d_hint(stage + C::kHalfBytes + b * C::kHalfBlock, &tm_y1, bars.y_full(s),
+                             64 * b, row0, u.bh, keep);
+          }
+          if (kKV) {
+            const size_t v0 = static_cast<size_t>(u.bh) * p.Npad + row0;
+            const uint32_t vec = sbase + C::kOffVec + s * C::kVecBytes;
+            bulk_load(vec, p.lse2 + v0, kBwdSub * 4, bars.y_full(s));
+            bulk_load(vec + kBwdSub * 4, p.dvec + v0, kBwdSub * 4, bars.y_full(s));
+          }
         }
-        issued = m + 1;
       }
-      // Drain: every copy issued must land before the CTA exits.
-      wait_bar_drain(bars.x_full(), 0, wctx);
+      // Drain: every copy issued must land before the CTA exits.  The last
+      // stage count in slot s is the largest one < yc congruent to s mod S.
+      if (nx > 0) wait_bar_drain(bars.x_full(), parity_of(nx - 1), wctx);
       for (int s = 0; s < S; ++s) {
-        if (issued > s) {
-          const int last = issued - 1 - ((issued - 1 - s) % S);
+        if (yc > static_cast<uint32_t>(s)) {
+          const uint32_t last = yc - 1 - ((yc - 1 - s) % S);
           wait_bar_drain(bars.y_full(s), parity_of(last / S), wctx);
         }
       }
@@ -445,11 +508,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (leader) umma_commit(bar);
       __syncwarp();
     };
-    // S and dP of sub-step m (TMEM buffer m & 1, ring stage m % S): X0 and X1
-    // against the 64 streamed rows of Y0 and Y1 in that stage.
-    auto issue_sdp = [&](int m) {
-      const int b = m & 1;
-      const uint32_t st = (m % S) * C::kStageBytes;
+    // S and dP into TMEM buffer b: X0 and X1 against the 64 streamed rows of
+    // Y0 and Y1 in ring slot `stage`.
+    auto issue_sdp = [&](int b, uint32_t stage) {
+      const uint32_t st = stage * C::kStageBytes;
       const uint32_t y0 = yk_lo + (st >> 4);
       const uint32_t y1 = yk_lo + ((st + C::kHalfBytes) >> 4);
       constexpr uint32_t x1 = C::kTileBytes >> 4;
@@ -478,15 +540,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
     };
-    // Accumulation of sub-step m over its 64 streamed rows, 16 per MMA; the
-    // A operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM buffer m & 1.
-    auto issue_acc = [&](int m) {
-      const int b = m & 1;
-      const uint32_t st = (m % S) * C::kStageBytes;
+    // Accumulation over the 64 streamed rows of ring slot `stage`, 16 per
+    // MMA; the A operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM
+    // buffer b.  `first`: the tile's first sub-step overwrites the accumulators.
+    auto issue_acc = [&](int b, uint32_t stage, bool first) {
+      const uint32_t st = stage * C::kStageBytes;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kBwdSub / 16; ++kk) {
-          const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
           const uint32_t r0 = (st + kk * 16 * 128) >> 4;
           const uint32_t r1 = (st + C::kHalfBytes + kk * 16 * 128) >> 4;
           // Slice kk (16 streamed rows) was packed by warpgroup kk into the
@@ -505,44 +567,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
     };
-    const int M = 2 * steps;
-    // The key-tile pass reads X from SMEM; the query-tile pass from TMEM,
-    // once the elementwise warps have copied it there.
-    bool ok = warp_wait_bar(kKV ? bars.x_full() : bars.x_tmem(), 0, wctx);
-    for (int m = 0; ok && m < 2; ++m) {
-      if (!warp_wait_bar(bars.y_full(m % S), parity_of(m / S), wctx)) {
-        ok = false;
-        break;
-      }
+    uint32_t gsub = 0;  // sub-steps (= Y stages) of earlier tiles
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int t = unit_index(r);
+      if (t >= total) break;
+      const Tile u = tile_at(t);
+      const int M = 2 * u.steps;
+      // The key-tile pass reads X from SMEM; the query-tile pass from TMEM,
+      // once the elementwise warps have copied it there.
+      if (!warp_wait_bar(kKV ? bars.x_full() : bars.x_tmem(), parity_of(r), wctx)) break;
       tc_fence_after_sync();
-      issue_sdp(m);
-      commit(bars.st_full(m));
-    }
-    for (int m = 0; ok && m < M; ++m) {
-      const int b = m & 1;
-      if (!warp_wait_bar(bars.p_full(b), parity_of(m >> 1), wctx)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      issue_acc(m);
-      commit(bars.y_empty(m % S));  // this sub-step's half tiles are consumed
-      const int m2 = m + 2;
-      if (m2 < M) {
-        // S, dP of sub-step m + 2 overwrite buffer b after the accumulation
-        // that reads it (MMAs of one thread run in issue order).
-        if (!warp_wait_bar(bars.y_full(m2 % S), parity_of(m2 / S), wctx)) {
+      // S, dP of sub-steps 0 and 1 overwrite buffers whose previous contents
+      // (the last tile's) are read by accumulations issued before them.
+      for (int m = 0; ok && m < 2 && m < M; ++m) {
+        const uint32_t gm = gsub + static_cast<uint32_t>(m);
+        if (!warp_wait_bar(bars.y_full(gm % S), parity_of(gm / S), wctx)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        issue_sdp(m2);
-        commit(bars.st_full(b));
+        issue_sdp(m, gm % S);
+        commit(bars.st_full(m));
+        if (kKV && m == M - 1) commit(bars.x_empty());  // X's last reader issued
       }
+      for (int m = 0; ok && m < M; ++m) {
+        const int b = m & 1;
+        const uint32_t gm = gsub + static_cast<uint32_t>(m);
+        if (!warp_wait_bar(bars.p_full(b), parity_of(gm >> 1), wctx) ||
+            (m == 0 && r > 0 && !warp_wait_bar(bars.acc_free(), parity_of(r - 1), wctx))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_acc(b, gm % S, m == 0);
+        commit(bars.y_empty(gm % S));  // this sub-step's half tiles are consumed
+        const int m2 = m + 2;
+        if (m2 < M) {
+          // S, dP of sub-step m + 2 overwrite buffer b after the accumulation
+          // that reads it (MMAs of one thread run in issue order).
+          const uint32_t gm2 = gsub + static_cast<uint32_t>(m2);
+          if (!warp_wait_bar(bars.y_full(gm2 % S), parity_of(gm2 / S), wctx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_sdp(b, gm2 % S);
+          commit(bars.st_full(b));
+          if (kKV && m2 == M - 1) commit(bars.x_empty());
+        }
+      }
+      if (!ok) break;
+      commit(bars.acc_done());  // the tile's accumulators are complete
+      gsub += static_cast<uint32_t>(M);
     }
-    // Every MMA issued has completed once acc_done fires.
-    commit(bars.acc_done());
-    wait_bar_drain(bars.acc_done(), 0, wctx);
+    // Every MMA issued has completed once mma_done fires.
+    commit(bars.mma_done());
+    wait_bar_drain(bars.mma_done(), 0, wctx);
   }
 
   // ------------------------------------------------------------ teardown
