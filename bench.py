@@ -82,6 +82,12 @@ NCU_TRAFFIC_BYTES_DECODE = {
 # Per-launch DRAM traffic of the forward kernel per workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
+# DRAM bytes (read + write) of one backward step (three launches), from an
+# ncu capture; a workload is left out until a capture of the kernels as
+# benchmarked exists.
+NCU_TRAFFIC_BYTES_BWD = {
+    "b2h16n4096d128_causal": 446_226_688,
+}
 NCU_TRAFFIC_BYTES = {
     "b2h16n4096d128_causal": 140_705_280,
     "b2h16n4096d256_causal": 579_028_224,
@@ -698,7 +704,9 @@ def run_ours_bwd(args, w):
                          "frac": achieved / peak,
                          "peak_source": f"{peaks_src} bf16_tflops (burst)",
                          "timed": "pre-pass, dK/dV pass and dQ pass together, per step",
-                         "traffic": None},
+                         # DRAM bytes of the three launches of one step (ncu, profiles/).
+                         "traffic": NCU_TRAFFIC_BYTES_BWD.get(w.name),
+                         "traffic_scope": "pre-pass + dK/dV pass + dQ pass, per step"},
             "cpu_baseline": cpu,
             "e2e": {"value": job_tflops(world, flops_step, e2e_steps, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
