@@ -69,20 +69,36 @@ def test_bwd_matches_oracle(fa, cuda_device, N, d, causal):
     check_grads(got, ref, f"N{N} d{d} c{causal}")
 
 
-def test_bwd_headline_shape_on_four_heads(fa, cuda_device):
-    """B=2, H=16, N=4096, d=128, causal: the GPU computes every head; four
-    heads (two per batch) are checked against the oracle in full."""
+@pytest.mark.parametrize("causal", [True, False])
+def test_bwd_headline_shape_on_four_heads(fa, cuda_device, causal):
+    """B=2, H=16, N=4096, d=128 (causal, and without the mask): the GPU
+    computes every head; four heads (two per batch) are checked against the
+    oracle in full."""
     w = workloads.HEADLINE
     q, k, v = workloads.generate(w)
     do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=1200)[0]
-    got = _grads(fa, cuda_device, q, k, v, do, w.causal, w.scale)
+    got = _grads(fa, cuda_device, q, k, v, do, causal, w.scale)
     heads = [(0, 0), (0, 9), (1, 4), (1, 15)]
 
     def pick(a):
         return np.stack([a[b, h] for b, h in heads])[None]
 
-    ref = oracle.attention_bwd(pick(q), pick(k), pick(v), pick(do), w.causal, w.scale)
-    check_grads([pick(g) for g in got], ref, w.name)
+    ref = oracle.attention_bwd(pick(q), pick(k), pick(v), pick(do), causal, w.scale)
+    check_grads([pick(g) for g in got], ref, f"{w.name} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_more_tiles_than_sms(fa, cuda_device, d, causal):
+    """160 tiles per pass on 152 SMs: the persistent grids give some CTAs a
+    second tile (the stationary tile reloaded, accumulators reused), every
+    head checked in full."""
+    q, k, v = workloads.generate_shape(1, 20, 1000, d, seed=1400 + d, qk_std=1.5)
+    do = workloads.generate_shape(1, 20, 1000, d, seed=1500 + d)[0]
+    scale = 1.0 / math.sqrt(d)
+    got = _grads(fa, cuda_device, q, k, v, do, causal, scale)
+    ref = oracle.attention_bwd(q, k, v, do, causal, scale)
+    check_grads(got, ref, f"H20 N1000 d{d} causal={causal}")
 
 
 def test_bwd_deterministic_and_workspace_checked(fa, cuda_device):
