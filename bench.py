@@ -604,9 +604,10 @@ def run_ours_bwd(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     fa.load_library()
+    elem = getattr(w, "dtype", "bf16")
     q, k, v = workloads.generate(w)
-    do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=5000 + w.seed)[0]
-    qd, kd, vd, dod = (workloads.as_torch(a).to(dev) for a in (q, k, v, do))
+    do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=5000 + w.seed, dtype=elem)[0]
+    qd, kd, vd, dod = (workloads.as_torch(a, elem).to(dev) for a in (q, k, v, do))
     o, lse = fa.attention_forward(qd, kd, vd, causal=w.causal, scale=w.scale)
     dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
     ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
@@ -645,8 +646,9 @@ def run_ours_bwd(args, w):
     clocks = sampler.stop() if sampler else None
 
     # End to end: Q, K, V, O, LSE, dO in from pinned host memory, dQ, dK, dV out.
-    hosts_in = [workloads.as_torch(a).pin_memory() for a in (q, k, v)]
-    hosts_in += [o.cpu().pin_memory(), lse.cpu().pin_memory(), workloads.as_torch(do).pin_memory()]
+    hosts_in = [workloads.as_torch(a, elem).pin_memory() for a in (q, k, v)]
+    hosts_in += [o.cpu().pin_memory(), lse.cpu().pin_memory(),
+                 workloads.as_torch(do, elem).pin_memory()]
     devs_in = [qd, kd, vd, o, lse, dod]
     hosts_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hosts_in)
@@ -684,7 +686,7 @@ def run_ours_bwd(args, w):
         if world == 1 and not args.skip_cpu_baseline:
             sl = [np.ascontiguousarray(a[:1, :1]) for a in (q, k, v, do)]
             t0 = time.perf_counter()
-            oracle.attention_bwd(*sl, w.causal, w.scale)
+            oracle.attention_bwd(*sl, w.causal, w.scale, dtype=elem)
             dt = time.perf_counter() - t0
             cpu = {"value": 2.5 * w.flops / (w.B * w.H) / dt / 1e12, "unit": UNIT,
                    "cores": 1, "kind": "oracle",
@@ -693,7 +695,7 @@ def run_ours_bwd(args, w):
         line = {
             "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": elem,
             "data": "synthetic",
             "config": {"workload": w.name, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "causal": w.causal, "scale": w.scale,
@@ -702,7 +704,9 @@ def run_ours_bwd(args, w):
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
-                         "peak_source": f"{peaks_src} bf16_tflops (burst)",
+                         "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
+                             "; fp16 x 1: its nominal dense rate equals bf16's"
+                             if elem == "f16" else ""),
                          "timed": "pre-pass, dK/dV pass and dQ pass together, per step",
                          # DRAM bytes of the three launches of one step (ncu, profiles/).
                          "traffic": NCU_TRAFFIC_BYTES_BWD.get(w.name),
@@ -748,8 +752,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     w = workloads.by_name(args.workload)
     if args.pass_ == "bwd":
-        if not isinstance(w, workloads.Workload) or w.dtype != "bf16" or w.d not in (64, 128):
-            ap.error("--pass bwd takes a bf16 square workload with d = 64 or 128")
+        if not isinstance(w, workloads.Workload) or w.d not in (64, 128):
+            ap.error("--pass bwd takes a square workload with d = 64 or 128")
         if args.impl == "reference":
             return run_reference_bwd(args, w)
         return run_ours_bwd(args, w)

@@ -212,7 +212,20 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
            int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Workspace bytes fa_bwd needs (0 on invalid arguments). */
+/*
+ * fa_bwd_ex — fa_bwd for either element type: q, k, v, o, dout, dq, dk, dv
+ * all hold `dtype` elements (FA_DTYPE_BF16 or FA_DTYPE_FP16: IEEE binary16
+ * bit patterns), the MMAs run on that type (P and dS rounded to it, as the
+ * forward rounds P) with fp32 accumulation; lse, the workspace and every
+ * other argument as for fa_bwd, which is fa_bwd_ex with FA_DTYPE_BF16.
+ * Returns FA_ERR_DTYPE for any other dtype, else as fa_bwd.
+ */
+int fa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const float *lse,
+              const void *dout, void *dq, void *dk, void *dv, int dtype, int B, int H, int N,
+              int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+              void *stream);
+
+/* Workspace bytes fa_bwd and fa_bwd_ex need (0 on invalid arguments). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*

@@ -249,3 +249,25 @@ def test_bwd_validation(lib):
     assert call(ws=9 * big) == FA_ERR_ALIAS        # workspace over dv
     if not torch.cuda.is_available():
         assert call() in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
+def test_bwd_ex_validation(lib):
+    """fa_bwd_ex: the element type is checked first; an fp16 call is
+    validated like a bf16 one."""
+    import torch
+
+    big = 1 << 24
+    base = [big, 2 * big, 3 * big, 4 * big, 5 * big, 6 * big, 7 * big, 8 * big, 9 * big]
+
+    def call(dtype, d=64, ws_bytes=1 << 20, q=big):
+        ptrs = [q] + base[1:]
+        return lib.fa_bwd_ex(*ptrs, dtype, 1, 2, 300, d, 1, 0.1, 10 * big, ws_bytes, None)
+
+    assert call(7) == FA_ERR_DTYPE
+    assert call(-1) == FA_ERR_DTYPE
+    assert call(1, q=0) == FA_ERR_NULL
+    assert call(1, d=96) == FA_ERR_HEAD_DIM
+    assert call(1, ws_bytes=6000) == FA_ERR_WORKSPACE
+    if not torch.cuda.is_available():
+        assert call(1) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+        assert call(0) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)

@@ -32,10 +32,10 @@ def fa(cuda_device):
     return fa
 
 
-def _grads(fa, dev, q, k, v, do, causal, scale):
+def _grads(fa, dev, q, k, v, do, causal, scale, dtype="bf16"):
     import torch
 
-    qd, kd, vd, dod = (workloads.as_torch(a).to(dev) for a in (q, k, v, do))
+    qd, kd, vd, dod = (workloads.as_torch(a, dtype).to(dev) for a in (q, k, v, do))
     o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=scale)
     dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
     torch.cuda.synchronize(dev)
@@ -117,3 +117,34 @@ def test_bwd_deterministic_and_workspace_checked(fa, cuda_device):
     with pytest.raises(fa.FAError) as err:
         fa.fa_bwd(qd, qd, qd, o, lse, qd, *grads, False, 0.1, small)
     assert err.value.code == 10
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [17, 129, 1000])
+def test_bwd_fp16_matches_oracle(fa, cuda_device, N, d, causal):
+    """fp16 inputs (fa_bwd_ex with FA_DTYPE_FP16): the oracle decodes the
+    same binary16 inputs exactly."""
+    q, k, v = workloads.generate_shape(1, 2, N, d, seed=1600 + N + d, qk_std=1.5, dtype="f16")
+    do = workloads.generate_shape(1, 2, N, d, seed=1700 + N + d, dtype="f16")[0]
+    scale = 1.0 / math.sqrt(d)
+    got = _grads(fa, cuda_device, q, k, v, do, causal, scale, dtype="f16")
+    ref = oracle.attention_bwd(q, k, v, do, causal, scale, dtype="f16")
+    check_grads(got, ref, f"fp16 N{N} d{d} c{causal}")
+
+
+def test_bwd_fp16_headline_shape_on_two_heads(fa, cuda_device):
+    """B=2, H=16, N=4096, d=128, causal, fp16: every head computed, two
+    checked against the oracle in full."""
+    w = workloads.by_name("b2h16n4096d128_causal_fp16")
+    q, k, v = workloads.generate(w)
+    do = workloads.generate_shape(w.B, w.H, w.N, w.d, seed=1800, dtype="f16")[0]
+    got = _grads(fa, cuda_device, q, k, v, do, w.causal, w.scale, dtype="f16")
+    heads = [(0, 3), (1, 12)]
+
+    def pick(a):
+        return np.stack([a[b, h] for b, h in heads])[None]
+
+    ref = oracle.attention_bwd(pick(q), pick(k), pick(v), pick(do), w.causal, w.scale,
+                               dtype="f16")
+    check_grads([pick(g) for g in got], ref, w.name)

@@ -83,6 +83,9 @@ def load_library(path: str | None = None):
         lib.fa_bwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
                                ctypes.c_size_t, vp]
+        lib.fa_bwd_ex.restype = i
+        lib.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp,
+                                  ctypes.c_size_t, vp]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_fwd_order_ablation.restype = i
@@ -312,27 +315,29 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, workspace=None,
            stream=None) -> None:
-    """Attention backward into preallocated CUDA tensors.
+    """Attention backward into preallocated CUDA tensors (C ABI ``fa_bwd_ex``).
 
-    q, k, v, o, dout, dq, dk, dv: contiguous ``torch.bfloat16`` ``[B, H, N, d]``
-    on one device; lse: ``torch.float32`` ``[B, H, N]`` (o and lse from
-    :func:`fa_fwd`).  ``workspace``: a CUDA byte tensor of at least
-    :func:`fa_bwd_workspace_bytes`; allocated here when None.
+    q, k, v, o, dout, dq, dk, dv: contiguous ``[B, H, N, d]`` CUDA tensors of one
+    element type, ``torch.bfloat16`` or ``torch.float16``, on one device; lse:
+    ``torch.float32`` ``[B, H, N]`` (o and lse from :func:`fa_fwd`).
+    ``workspace``: a CUDA byte tensor of at least :func:`fa_bwd_workspace_bytes`;
+    allocated here when None.
     """
     import torch
 
     B, H, N, d = _dims(q)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q must be torch.bfloat16 or torch.float16")
+    elem = q.dtype
     for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
                     ("dv", dv)):
         if tuple(t.shape) != (B, H, N, d):
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(B, H, N, d)}")
     if tuple(lse.shape) != (B, H, N):
         raise ValueError(f"lse has shape {tuple(lse.shape)}, expected {(B, H, N)}")
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
-                        ("v", v, torch.bfloat16), ("o", o, torch.bfloat16),
-                        ("dout", dout, torch.bfloat16), ("dq", dq, torch.bfloat16),
-                        ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16),
-                        ("lse", lse, torch.float32)):
+    for name, t, dt in (("q", q, elem), ("k", k, elem), ("v", v, elem), ("o", o, elem),
+                        ("dout", dout, elem), ("dq", dq, elem), ("dk", dk, elem),
+                        ("dv", dv, elem), ("lse", lse, torch.float32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
             raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor on q's device")
     with torch.cuda.device(q.device):
@@ -344,12 +349,13 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, worksp
         if stream is None:
             stream = torch.cuda.current_stream(q.device)
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-        rc = load_library().fa_bwd(
+        dtype = FA_DTYPE_FP16 if elem == torch.float16 else FA_DTYPE_BF16
+        rc = load_library().fa_bwd_ex(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dtype, B, H, N, d,
             int(bool(causal)), float(scale), workspace.data_ptr(),
             workspace.numel() * workspace.element_size(), handle or None)
-        _check(rc, "fa_bwd")
+        _check(rc, "fa_bwd_ex")
 
 
 def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,

@@ -80,14 +80,21 @@ bool configure_dim() {
 
 // As for the forward: the register split (setmaxnreg) assumes the launch
 // register count.
-template <int D, bool kKV>
-cudaError_t configure_bwd_kernel() {
+template <int D, bool kKV, bool kF16>
+cudaError_t configure_bwd_one() {
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_bwd_kernel<D, kKV>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, fa::fa_bwd_kernel<D, kKV, kF16>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != static_cast<int>(fa::kBwdLaunchRegs)) return cudaErrorInvalidKernelImage;
-  return cudaFuncSetAttribute(fa::fa_bwd_kernel<D, kKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fa::fa_bwd_kernel<D, kKV, kF16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::BwdCfg<D, kKV>::kSmemAlloc));
+}
+
+template <int D, bool kKV>
+cudaError_t configure_bwd_kernel() {
+  const cudaError_t e = configure_bwd_one<D, kKV, false>();
+  return e != cudaSuccess ? e : configure_bwd_one<D, kKV, true>();
 }
 
 template <int D, bool kV1>
@@ -151,7 +158,8 @@ int prepare_device(int* dev_out, int* sms_out) {
 
 // Contiguous [BH][N][d] bf16 viewed as a 3-D tensor (d innermost), boxes of
 // 64 columns x `box_rows` rows x 1 slice with the 128-byte swizzle (split-KV).
-bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128) {
+bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128,
+                CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
@@ -159,7 +167,7 @@ bool encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUresult r =
-      g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+      g_encode(map, type, 3, const_cast<void*>(ptr), dims, strides, box,
                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -382,7 +390,7 @@ int64_t bwd_npad(int N) { return (static_cast<int64_t>(N) + fa::kBwdTile - 1) / 
 // Three launches on one stream: D and LSE*log2(e) into the workspace, the
 // dK/dV pass (prm_kv: out0 = dK, out1 = dV), the dQ pass (prm_q: out0 = dQ).
 // mX: 128-row boxes (stationary tiles); mX64: 64-row boxes (streamed halves).
-template <int D>
+template <int D, bool kF16>
 int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensorMap& mq,
                const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                const CUtensorMap& mq64, const CUtensorMap& mk64, const CUtensorMap& mv64,
@@ -390,17 +398,17 @@ int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensor
                int sms, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(base.num_bh) * base.Npad;
   const int64_t threads = rows * (D / 8);  // a multiple of 256: Npad is a multiple of 128
-  fa::fa_bwd_prep_kernel<D><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
+  fa::fa_bwd_prep_kernel<D, kF16><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
       const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   // Persistent grids: one CTA per SM (at most one per tile) walks the tiles.
   const unsigned ctas = static_cast<unsigned>(
       std::min<int64_t>(static_cast<int64_t>(base.T) * base.num_bh, sms));
-  fa::fa_bwd_kernel<D, true><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, true>::kSmemAlloc, stream>>>(
+  fa::fa_bwd_kernel<D, true, kF16><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, true>::kSmemAlloc, stream>>>(
       mk, mv, mq64, mdo64, base);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa::fa_bwd_kernel<D, false><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, false>::kSmemAlloc, stream>>>(
+  fa::fa_bwd_kernel<D, false, kF16><<<ctas, fa::kBwdThreads, fa::BwdCfg<D, false>::kSmemAlloc, stream>>>(
       mq, mdo, mk64, mv64, prm_q);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -417,7 +425,16 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                       int causal, float scale, void* workspace, size_t workspace_bytes,
                       void* stream) {
+  return fa_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, FA_DTYPE_BF16, B, H, N, d, causal, scale,
+                   workspace, workspace_bytes, stream);
+}
+
+extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         int dtype, int B, int H, int N, int d, int causal, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
   if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1)) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
   const int64_t BH = static_cast<int64_t>(B) * H;
@@ -453,11 +470,14 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if (g_encode == nullptr) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mdo, mq64, mk64, mv64, mdo64;
   const int bhi = static_cast<int>(BH);
-  if (!encode_map(&mq, q, bhi, N, d) || !encode_map(&mk, k, bhi, N, d) ||
-      !encode_map(&mv, v, bhi, N, d) || !encode_map(&mdo, dout, bhi, N, d) ||
-      !encode_map(&mq64, q, bhi, N, d, fa::kBwdSub) || !encode_map(&mk64, k, bhi, N, d, fa::kBwdSub) ||
-      !encode_map(&mv64, v, bhi, N, d, fa::kBwdSub) ||
-      !encode_map(&mdo64, dout, bhi, N, d, fa::kBwdSub))
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  const CUtensorMapDataType tt =
+      f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int rows = 128, half = fa::kBwdSub;
+  if (!encode_map(&mq, q, bhi, N, d, rows, tt) || !encode_map(&mk, k, bhi, N, d, rows, tt) ||
+      !encode_map(&mv, v, bhi, N, d, rows, tt) || !encode_map(&mdo, dout, bhi, N, d, rows, tt) ||
+      !encode_map(&mq64, q, bhi, N, d, half, tt) || !encode_map(&mk64, k, bhi, N, d, half, tt) ||
+      !encode_map(&mv64, v, bhi, N, d, half, tt) || !encode_map(&mdo64, dout, bhi, N, d, half, tt))
     return FA_ERR_LAUNCH;
 
   fa::BwdParams prm;
@@ -478,10 +498,15 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   prm_q.out0 = static_cast<uint16_t*>(dq);
   prm_q.out1 = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_bwd<64>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
-                                  prm_q, sms, st)
-                 : launch_bwd<128>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
-                                   prm_q, sms, st);
+  if (f16)
+    return d == 64 ? launch_bwd<64, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                                          prm, prm_q, sms, st)
+                   : launch_bwd<128, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                                           prm, prm_q, sms, st);
+  return d == 64 ? launch_bwd<64, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                                         prm, prm_q, sms, st)
+                 : launch_bwd<128, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                                          prm, prm_q, sms, st);
 }
 
 // ------------------------------------------------------- loop-order ablation

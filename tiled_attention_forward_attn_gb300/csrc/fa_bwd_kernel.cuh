@@ -19,7 +19,7 @@
 //                         tile i the tensor core computes S^T = K_j Q_i^T
 //                         and dP^T = V_j dO_i^T into TMEM, four warps (one
 //                         key row = one TMEM lane each) turn them into P^T
-//                         and dS^T (bf16 pairs written back over them), and
+//                         and dS^T (16-bit pairs written back over them), and
 //                         dV_j += P^T dO_i, dK_j += dS^T Q_i accumulate in
 //                         TMEM with P^T / dS^T read straight from TMEM;
 //   fa_bwd_kernel<D,false> one CTA per (batch*head, 128-query tile i): Q_i
@@ -71,7 +71,7 @@ constexpr int kBwdSub = 64;    // streamed rows per sub-step
 constexpr int kBwdEwCols = kBwdSub / 4;  // columns of a sub-step per elementwise warpgroup
 
 struct BwdParams {
-  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][D] bf16
+  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][D] bf16 or fp16
   uint16_t* out1;     // key-tile pass: dV; unused otherwise
   const float* lse2;  // [BH][Npad] -LSE * log2(e) per query (0 past N)
   const float* dvec;  // [BH][Npad] -rowsum(dO * O) per query (0 past N)
@@ -109,11 +109,11 @@ struct BwdCfg {
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "dynamic shared memory per block");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;      // S buffer b at 64b; then P^T or dS as bf16 pairs
+  static constexpr uint32_t kColS = 0;      // S buffer b at 64b; then P^T or dS as 16-bit pairs
   static constexpr uint32_t kColDP = 128;   // dP buffer b at 128 + 64b; then dS^T (key-tile pass)
   static constexpr uint32_t kColAcc0 = 256;      // dK (key-tile pass) or dQ
   static constexpr uint32_t kColAcc1 = 256 + D;  // dV (key-tile pass)
-  // Query-tile pass: Q_i and dO_i as bf16 pairs in the spare columns, so
+  // Query-tile pass: Q_i and dO_i as 16-bit pairs in the spare columns, so
   // the S and dP MMAs read their A operand from TMEM and only K/V from SMEM.
   static constexpr uint32_t kColXT = 384;
   static_assert(kKV || kColXT + D <= kTmemCols, "Q and dO pairs fit in TMEM");
@@ -140,7 +140,7 @@ struct BwdBars {
 // -D_i = -rowsum(dO_i * O_i) and -LSE_i * log2(e) for every row of the
 // padded [BH][Npad] layout (0 past N), negated for the elementwise pass's
 // fused multiply-adds.  D/8 threads per row, 16 bytes each.
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ lse2,
@@ -159,8 +159,8 @@ __global__ void __launch_bounds__(256)
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
-      acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+      acc = fmaf(elem_to_f32<kF16>(aw[e], false), elem_to_f32<kF16>(bw[e], false), acc);
+      acc = fmaf(elem_to_f32<kF16>(aw[e], true), elem_to_f32<kF16>(bw[e], true), acc);
     }
   }
 #pragma unroll
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(256)
 
 // kKV = true: X = (K, V) of key tile xt, Y = (Q, dO) of query tiles.
 // kKV = false: X = (Q, dO) of query tile xt, Y = (K, V) of key tiles.
-template <int D, bool kKV>
+template <int D, bool kKV, bool kF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
                   const __grid_constant__ CUtensorMap tm_y0, const __grid_constant__ CUtensorMap tm_y1,
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int x_idx = xt * kBwdTile + row;  // key (kKV) or query index of this row
       if (!kKV) {
         // Warpgroups 0 and 1 copy this row of X_g (g = 0: Q_i, 1: dO_i) from the swizzled SMEM
-        // tile into TMEM as bf16 pairs: 16-byte chunk c of the row sits in
+        // tile into TMEM as 16-bit pairs: 16-byte chunk c of the row sits in
         // 64-column block c / 8 at row * 128 + ((c % 8) ^ (row % 8)) * 16.  The
         // previous tile's S/dP MMAs, the only readers of these columns, are
         // complete: its last st_full was consumed.
@@ -367,8 +367,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fadd2(t0, t1, __uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1]), nd[h],
                   nd[h + 1]);
             fmul2(d0, d1, p0, p1, t0, t1);
-            pp[(e + h) / 2] = pack_bf16x2(p0, p1);
-            pd[(e + h) / 2] = pack_bf16x2(d0, d1);
+            pp[(e + h) / 2] = pack_x2<kF16>(p0, p1);
+            pd[(e + h) / 2] = pack_x2<kF16>(d0, d1);
           }
         }
         // The pairs go into the first 8 of this warpgroup's 16 columns, which
@@ -422,8 +422,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          w4[e] = pack_bf16x2(__uint_as_float(racc[8 * q8 + 2 * e]) * mul,
-                              __uint_as_float(racc[8 * q8 + 2 * e + 1]) * mul);
+          w4[e] = pack_x2<kF16>(__uint_as_float(racc[8 * q8 + 2 * e]) * mul,
+                                __uint_as_float(racc[8 * q8 + 2 * e + 1]) * mul);
         if (in_range) dst[q8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
     }
@@ -491,8 +491,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     const bool leader = elect_one_sync();
     constexpr uint32_t kHi = desc_hi_sw128(1024);
-    constexpr uint32_t kIdescSS = idesc_bf16_f32(kBwdTile, kBwdSub, 0, 0);
-    constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBwdTile, D, 0, 1);
+    // Both operands of every MMA share the element type (P, dS included).
+    constexpr uint32_t kIdescSS = kF16 ? idesc_f16_f32(kBwdTile, kBwdSub, 0, 0)
+                                       : idesc_bf16_f32(kBwdTile, kBwdSub, 0, 0);
+    constexpr uint32_t kIdescAcc = kF16 ? idesc_f16_f32(kBwdTile, D, 0, 1)
+                                        : idesc_bf16_f32(kBwdTile, D, 0, 1);
     const uint32_t x_lo = desc_lo(sX, 16);               // X tiles, K-major A
     const uint32_t yk_lo = desc_lo(sY, 16);              // Y tiles, K-major B
     const uint32_t ymn_lo = desc_lo(sY, C::kHalfBlock);  // Y halves, MN-major B
@@ -541,7 +544,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
     };
     // Accumulation over the 64 streamed rows of ring slot `stage`, 16 per
-    // MMA; the A operand (P^T / dS^T / dS as bf16 pairs) comes from TMEM
+    // MMA; the A operand (P^T / dS^T / dS as 16-bit pairs) comes from TMEM
     // buffer b.  `first`: the tile's first sub-step overwrites the accumulators.
     auto issue_acc = [&](int b, uint32_t stage, bool first) {
       const uint32_t st = stage * C::kStageBytes;

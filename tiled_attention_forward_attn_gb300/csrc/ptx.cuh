@@ -394,6 +394,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// The 16-bit element in the low (hi = false) or high half of a word, as fp32
+// (bf16: the bits shifted into place; fp16: converted exactly).
+template <bool kF16>
+__device__ __forceinline__ float elem_to_f32(uint32_t w, bool hi) {
+  const uint32_t bits = hi ? (w >> 16) : (w & 0xFFFFu);
+  if (!kF16) return __uint_as_float(bits << 16);
+  float f;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(bits));
+  return f;
+}
+
 // Two fp32 values to one 16-bit pair of the element type (bf16 or fp16).
 template <bool kF16>
 __device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
