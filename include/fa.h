@@ -103,6 +103,38 @@ int fa_fwd_strided(const void *q, const int64_t *q_strides, const void *k,
                    int causal, float scale, void *stream);
 
 /*
+ * fa_fwd_host — the forward of fa_fwd for inputs and outputs in HOST
+ * memory, the one entry point that copies: on `stream` it queues the copies
+ * of q, k, v into the caller's device workspace (one cudaMemcpyAsync each),
+ * the forward kernel, and the copies of O and LSE back.  The pages' method
+ * has no counterpart; it is the end-to-end path of a caller whose tensors
+ * live on the host.
+ *
+ *   q_host, k_host, v_host : const [B][H][N][d] elements of `dtype`
+ *                            (FA_DTYPE_BF16 / FA_DTYPE_FP16), contiguous, host
+ *   o_host                 : [B][H][N][d] of `dtype`, host, written
+ *   lse_host               : fp32 [B][H][N], host, written
+ *   d, causal, scale       : as for fa_fwd_strided
+ *   workspace              : device memory of at least
+ *                            fa_fwd_host_workspace_bytes() bytes, 256-byte
+ *                            aligned, owned by the caller (Q, K, V, O and LSE
+ *                            staged there, overwritten)
+ * Page-locked host memory lets the copies run asynchronously at full
+ * bandwidth; pageable memory works, with the driver's staging.  The host
+ * outputs hold the result once `stream` has been synchronised; the host
+ * inputs must stay unchanged until then.  Host outputs must not overlap a
+ * host input or each other (FA_ERR_ALIAS).  Everything fa_fwd would reject
+ * is rejected before any copy is queued; FA_ERR_WORKSPACE when the
+ * workspace is missing or small.
+ */
+int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host,
+                float *lse_host, int dtype, int B, int H, int N, int d, int causal, float scale,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Device workspace bytes fa_fwd_host needs (0 on invalid arguments). */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * fa_fwd_splitkv — attention of a short block of queries against a long key
  * sequence (decode), split over the keys.
  *

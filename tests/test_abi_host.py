@@ -271,3 +271,31 @@ def test_bwd_ex_validation(lib):
     if not torch.cuda.is_available():
         assert call(1) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
         assert call(0) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
+def test_fwd_host_validation(lib):
+    """fa_fwd_host rejects bad arguments before queueing any copy (no GPU
+    needed for these checks)."""
+    import torch
+
+    big = 1 << 24
+    need = lib.fa_fwd_host_workspace_bytes(1, 2, 300, 64)
+    # Q, K, V, O: 2 heads x 300 rows x 64 x 2 bytes, rounded to 256; LSE 2400 -> 2560
+    assert need == 4 * 76800 + 2560
+    assert lib.fa_fwd_host_workspace_bytes(1, 2, 300, 72) == 0
+
+    def call(q=big, o=4 * big, lse=5 * big, dtype=0, d=64, causal=1, ws=1 << 30,
+             ws_bytes=1 << 22):
+        return lib.fa_fwd_host(q, 2 * big, 3 * big, o, lse, dtype, 1, 2, 300, d, causal, 0.1, ws,
+                               ws_bytes, None)
+
+    assert call(q=0) == FA_ERR_NULL
+    assert call(dtype=5) == FA_ERR_DTYPE
+    assert call(d=72) == FA_ERR_HEAD_DIM
+    assert call(causal=2) == FA_ERR_SHAPE
+    assert call(ws_bytes=need - 1) == FA_ERR_WORKSPACE
+    assert call(ws=(1 << 30) + 16) == FA_ERR_ALIGN
+    assert call(o=big + 64) == FA_ERR_ALIAS          # O over Q
+    assert call(lse=4 * big + 256) == FA_ERR_ALIAS   # LSE inside O
+    if not torch.cuda.is_available():
+        assert call() in (FA_ERR_LAUNCH, FA_ERR_DEVICE)

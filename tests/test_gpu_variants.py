@@ -246,3 +246,28 @@ def test_output_rows_16_byte_aligned_only(fa, cuda_device, offset, pad, d):
     o_ref, lse_ref = oracle.attention(q, k, v, True, 0.09)
     compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
             label=f"o offset {offset} pad {pad}")
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("bf16", 256)])
+def test_host_buffers_match_oracle(fa, cuda_device, dtype, d, pinned):
+    """fa_fwd_host: Q, K, V in host memory (page-locked or pageable), O and
+    LSE written back to host memory; two calls in a row on one workspace."""
+    import torch
+
+    B, H, N = 1, 2, 300
+    scale = 1.0 / math.sqrt(d)
+    ws = torch.empty(fa.fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                     device=cuda_device)
+    for seed in (740, 741):
+        q, k, v = workloads.generate_shape(B, H, N, d, seed=seed + d, qk_std=1.5, dtype=dtype)
+        hq, hk, hv = (workloads.as_torch(a, dtype) for a in (q, k, v))
+        ho = torch.empty_like(hq)
+        hl = torch.empty((B, H, N), dtype=torch.float32)
+        if pinned:
+            hq, hk, hv, ho, hl = (t.pin_memory() for t in (hq, hk, hv, ho, hl))
+        fa.fa_fwd_host(hq, hk, hv, ho, hl, True, scale, ws)
+        torch.cuda.synchronize(cuda_device)
+        o_ref, lse_ref = oracle.attention(q, k, v, True, scale, dtype=dtype)
+        compare(ho.float().numpy(), hl.numpy(), o_ref, lse_ref,
+                label=f"host {dtype} d{d} pinned={pinned} seed {seed}")

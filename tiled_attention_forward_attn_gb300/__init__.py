@@ -18,6 +18,7 @@ from . import _build
 
 __all__ = [
     "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version", "fa_fwd_strided",
+    "fa_fwd_host", "fa_fwd_host_workspace_bytes",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
     "fa_bwd", "fa_bwd_workspace_bytes", "attention_backward", "attention_forward_order_ablation",
@@ -61,6 +62,11 @@ def load_library(path: str | None = None):
         lib.fa_fwd_strided.restype = i
         lib.fa_fwd_strided.argtypes = [vp, i64p, vp, i64p, vp, i64p, vp, i64p, vp, i, i, i, i, i,
                                        i, f, vp]
+        lib.fa_fwd_host.restype = i
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, ctypes.c_size_t,
+                                    vp]
+        lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_strerror.argtypes = [i]
         lib.fa_get_device_status.restype = i
@@ -191,6 +197,46 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
         _check(fa_fwd_strided(q.data_ptr(), st(q), k.data_ptr(), st(k), v.data_ptr(), st(v),
                               o.data_ptr(), st(o), lse.data_ptr(), dtype, B, H, N, d, causal,
                               scale, handle), "fa_fwd")
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Device workspace bytes fa_fwd_host needs (0 on invalid arguments)."""
+    return int(load_library().fa_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_host(q, k, v, o, lse, causal: bool, scale: float, workspace, stream=None) -> None:
+    """Forward with host tensors (C ABI ``fa_fwd_host``): copies Q, K, V into
+    ``workspace`` on the device, runs the forward and copies O and LSE back,
+    all queued on ``stream``; synchronise it before reading ``o``, ``lse``.
+
+    q, k, v, o: contiguous CPU tensors ``[B, H, N, d]`` of one type
+    (``torch.bfloat16`` or ``torch.float16``; page-locked for asynchronous
+    copies); lse: contiguous CPU ``torch.float32`` ``[B, H, N]``; workspace: a
+    CUDA byte tensor of at least :func:`fa_fwd_host_workspace_bytes` bytes
+    (its device is the one used).
+    """
+    import torch
+
+    B, H, N, d = _dims(q)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q must be torch.bfloat16 or torch.float16")
+    for name, t, dt, shape in (("k", k, q.dtype, (B, H, N, d)), ("v", v, q.dtype, (B, H, N, d)),
+                               ("o", o, q.dtype, (B, H, N, d)), ("lse", lse, torch.float32, (B, H, N)),
+                               ("q", q, q.dtype, (B, H, N, d))):
+        if tuple(t.shape) != shape or t.dtype != dt or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of shape {shape}")
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    with torch.cuda.device(workspace.device):
+        if stream is None:
+            stream = torch.cuda.current_stream(workspace.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        dtype = FA_DTYPE_FP16 if q.dtype == torch.float16 else FA_DTYPE_BF16
+        rc = load_library().fa_fwd_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dtype,
+            B, H, N, d, int(bool(causal)), float(scale), workspace.data_ptr(),
+            workspace.numel(), handle or None)
+        _check(rc, "fa_fwd_host")
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

@@ -373,6 +373,66 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
                   causal, scale, stream);
 }
 
+namespace {
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  if (d != 256 && (d < 16 || d > 128 || d % 16 != 0)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return 4 * round256(rows * d * 2) + round256(rows * 4);
+}
+
+extern "C" int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                           void* o_host, float* lse_host, int dtype, int B, int H, int N, int d,
+                           int causal, float scale, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  // Everything fa_fwd would reject is rejected here, before any copy is queued.
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host) return FA_ERR_NULL;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_SHAPE;
+  if (d != 256 && (d < 16 || d > 128 || d % 16 != 0)) return FA_ERR_HEAD_DIM;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t unit_rows = d == 256 ? fa::kW_TileM : fa::kUnitM;
+  const int64_t num_units = (static_cast<int64_t>(N) + unit_rows - 1) / unit_rows;
+  if (BH > INT_MAX || BH * num_units > INT_MAX || BH * N > INT_MAX) return FA_ERR_SHAPE;
+  const size_t need = fa_fwd_host_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  const size_t tb = static_cast<size_t>(BH) * N * d * 2;
+  const size_t lb = static_cast<size_t>(BH) * N * 4;
+  // The outputs overlap neither an input nor each other (host ranges).
+  const void* hin[3] = {q_host, k_host, v_host};
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(o_host, tb, hin[i], tb) || overlaps(lse_host, lb, hin[i], tb)) return FA_ERR_ALIAS;
+  if (overlaps(o_host, tb, lse_host, lb)) return FA_ERR_ALIAS;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t t = round256(tb);
+  void* qd = ws;
+  void* kd = ws + t;
+  void* vd = ws + 2 * t;
+  void* od = ws + 3 * t;
+  float* ld = reinterpret_cast<float*>(ws + 4 * t);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(qd, q_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(kd, k_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(vd, v_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const int rc = fwd_impl(qd, nullptr, kd, nullptr, vd, nullptr, od, nullptr, ld, dtype, B, H, N,
+                          d, causal, scale, stream);
+  if (rc != FA_OK) return rc;
+  if (cudaMemcpyAsync(o_host, od, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(lse_host, ld, lb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
 extern "C" int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k,
                               const int64_t* k_strides, const void* v, const int64_t* v_strides,
                               void* o, const int64_t* o_strides, float* lse, int dtype, int B,
