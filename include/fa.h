@@ -313,8 +313,12 @@ int fa_set_wait_limit_ns(unsigned long long ns);
 /*
  * Test hook: a bit set of FA_INJECT_* faults applied by later calls,
  * process-wide (0 = none, the default).  FA_INJECT_SKIP_FIRST_V_LOAD makes
- * every CTA skip its first V-tile copy, so a wait runs out and the call ends
- * with FA_DEVICE_STATUS_TIMEOUT set.  For tests of the failure path only.
+ * every CTA skip one streamed-tile copy — the first V tile of fa_fwd /
+ * fa_fwd_strided / fa_fwd_host (every head dimension), the first K/V tile of
+ * the split-KV pass, the first streamed stage of each fa_bwd pass — so a wait
+ * runs out and the call ends with FA_DEVICE_STATUS_TIMEOUT set.  No GPU
+ * fault is involved: the kernels drain what they issued, free TMEM and exit.
+ * For tests of the failure path only.
  */
 #define FA_INJECT_SKIP_FIRST_V_LOAD 1u
 int fa_set_fault_injection(unsigned int flags);

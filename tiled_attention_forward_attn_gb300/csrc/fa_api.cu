@@ -554,6 +554,7 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.scale = scale;
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.inject = g_inject.load(std::memory_order_relaxed);
   fa::BwdParams prm_q = prm;
   prm_q.out0 = static_cast<uint16_t*>(dq);
   prm_q.out1 = nullptr;
@@ -815,6 +816,7 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   prm.causal = causal;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.inject = g_inject.load(std::memory_order_relaxed);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return d == 64 ? launch_split<64>(mk, mv, prm, s, true) : launch_split<128>(mk, mv, prm, s, true);
 }
@@ -913,6 +915,7 @@ extern "C" int fa_fwd_splitkv_static(const void* q, const void* k, const void* v
   prm.causal = causal;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.inject = g_inject.load(std::memory_order_relaxed);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Always the two-pass form: this entry point's partials go through its
   // built-in scratch array.

@@ -83,6 +83,7 @@ struct BwdParams {
   float scale_log2;   // scale * log2(e)
   float scale;        // the softmax scale
   uint64_t wait_limit_ns;
+  uint32_t inject = 0;  // test hooks (0 in normal use)
 };
 
 template <int D, bool kKV>
@@ -461,6 +462,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const int row0 = (u.y_first + (m >> 1)) * kBwdTile + kBwdSub * (m & 1);
           const uint32_t stage = sY + s * C::kStageBytes;
+          // Test hook: the first streamed stage is never copied, so its wait
+          // must time out.
+          if (yc == 0 && (p.inject & kInjectSkipFirstV)) continue;
           mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes + C::kVecBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b) {
@@ -483,7 +487,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int s = 0; s < S; ++s) {
         if (yc > static_cast<uint32_t>(s)) {
           const uint32_t last = yc - 1 - ((yc - 1 - s) % S);
-          wait_bar_drain(bars.y_full(s), parity_of(last / S), wctx);
+          if (!(last == 0 && (p.inject & kInjectSkipFirstV)))
+            wait_bar_drain(bars.y_full(s), parity_of(last / S), wctx);
         }
       }
     }

@@ -362,19 +362,25 @@ __global__ void __launch_bounds__(kW_Threads, 1)
     if (lane == 0) {
       const uint64_t keep = make_l2_policy_evict_last();
       const uint64_t once = make_l2_policy_evict_first();
-      uint32_t ic = 0, qc = 0;  // K/V items and Q tiles issued so far
+      uint32_t ic = 0, qc = 0;  // K/V items and Q tiles issued (or skipped) so far
+      int64_t skipped = -1;     // test hook: the item never issued
+      bool v_seen = false;
       int cur_h = 0, cur_b = 0;
       // One K or V tile into the next ring slot, once that slot is free.
-      auto issue = [&](const CUtensorMap* map, int row0) -> bool {
+      auto issue = [&](const CUtensorMap* map, int row0, bool skip) -> bool {
         const int s = static_cast<int>(ic % R);
         if (ic >= static_cast<uint32_t>(R) &&
             !wait_bar(bars.kv_empty(s), parity_of(ic / R - 1), wctx))
           return false;
-        mbar_arrive_expect_tx(bars.kv_full(s), C::kKVBytes);
+        if (skip) {
+          skipped = ic;
+        } else {
+          mbar_arrive_expect_tx(bars.kv_full(s), C::kKVBytes);
 #pragma unroll
-        for (int b = 0; b < kW_D / 64; ++b)
-          tma_load_4d_hint(sRing + s * C::kKVBytes + b * C::kKVBlock, map, bars.kv_full(s), 64 * b,
-                           row0, cur_h, cur_b, keep);
+          for (int b = 0; b < kW_D / 64; ++b)
+            tma_load_4d_hint(sRing + s * C::kKVBytes + b * C::kKVBlock, map, bars.kv_full(s),
+                             64 * b, row0, cur_h, cur_b, keep);
+        }
         ++ic;
         return true;
       };
@@ -393,9 +399,13 @@ __global__ void __launch_bounds__(kW_Threads, 1)
           tma_load_4d_hint(sQ + b * C::kQBlock, &tm_q, bars.q_full(), 64 * b, u.q0, u.h, u.b, once);
         ++qc;
         // Items in the order the MMAs read them: K_0, K_1, then V_j, K_j+2.
-        bool ok = issue(&tm_k, 0) && (u.n < 2 || issue(&tm_k, kW_BlockN));
-        for (int j = 0; ok && j < u.n; ++j)
-          ok = issue(&tm_v, j * kW_BlockN) && (j + 2 >= u.n || issue(&tm_k, (j + 2) * kW_BlockN));
+        bool ok = issue(&tm_k, 0, false) && (u.n < 2 || issue(&tm_k, kW_BlockN, false));
+        for (int j = 0; ok && j < u.n; ++j) {
+          const bool skip = !v_seen && (p.inject & kInjectSkipFirstV);
+          v_seen = true;
+          ok = issue(&tm_v, j * kW_BlockN, skip) &&
+               (j + 2 >= u.n || issue(&tm_k, (j + 2) * kW_BlockN, false));
+        }
         if (!ok) break;
       }
       // Drain: every copy issued must land before the CTA may exit.  The last
@@ -404,7 +414,8 @@ __global__ void __launch_bounds__(kW_Threads, 1)
       for (int s = 0; s < R; ++s) {
         if (ic > static_cast<uint32_t>(s)) {
           const uint32_t last = ic - 1 - ((ic - 1 - s) % R);
-          wait_bar_drain(bars.kv_full(s), parity_of(last / R), wctx);
+          if (static_cast<int64_t>(last) != skipped)
+            wait_bar_drain(bars.kv_full(s), parity_of(last / R), wctx);
         }
       }
     }

@@ -64,6 +64,7 @@ struct SplitParams {
   int Nq, Nk, num_bh, splits, keys_per_split, causal;
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  uint32_t inject = 0;  // test hooks (0 in normal use)
 };
 
 template <int D>
@@ -185,21 +186,26 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
           break;
         const int k0 = k_begin + t * kSplitTileKeys;
         const uint32_t stage = sbase + s * C::kStageBytes;
-        mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
+        // Test hook: the first K/V tile is never copied, so its wait must time out.
+        if (!(t == 0 && (p.inject & kInjectSkipFirstV))) {
+          mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
 #pragma unroll
-        for (int b = 0; b < D / 64; ++b) {
-          tma_load_3d_hint(stage + b * C::kBoxBytes, &tm_k, bar_full + 8 * s, 64 * b, k0, bh, policy);
-          tma_load_3d_hint(stage + C::kTileBytes + b * C::kBoxBytes, &tm_v, bar_full + 8 * s, 64 * b,
-                           k0, bh, policy);
+          for (int b = 0; b < D / 64; ++b) {
+            tma_load_3d_hint(stage + b * C::kBoxBytes, &tm_k, bar_full + 8 * s, 64 * b, k0, bh,
+                             policy);
+            tma_load_3d_hint(stage + C::kTileBytes + b * C::kBoxBytes, &tm_v, bar_full + 8 * s,
+                             64 * b, k0, bh, policy);
+          }
         }
         issued = t + 1;
       }
       // Drain: the last copy into each stage must land before the CTA exits
-      // or the ring is reused by the merge.
+      // or the ring is reused by the merge (the skipped one never lands).
       for (int s = 0; s < kS; ++s) {
         if (issued > s) {
           const int last = issued - 1 - ((issued - 1 - s) % kS);
-          split_wait(bar_full + 8 * s, static_cast<uint32_t>(last / kS) & 1u, p.wait_limit_ns);
+          if (!(last == 0 && (p.inject & kInjectSkipFirstV)))
+            split_wait(bar_full + 8 * s, static_cast<uint32_t>(last / kS) & 1u, p.wait_limit_ns);
         }
       }
     }
