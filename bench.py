@@ -76,8 +76,8 @@ class L2Flush:
 # from one ncu capture per workload (profiles/); a workload is left out
 # until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES_DECODE = {
-    "decode_b4h16q16k16384d128_causal": 540_464_384,
-    "decode_b4h16q1k16384d128": 538_349_056,
+    "decode_b4h16q16k16384d128_causal": 538_642_816,
+    "decode_b4h16q1k16384d128": 538_550_528,
 }
 # Per-launch DRAM traffic of the forward kernel per workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
@@ -86,11 +86,11 @@ NCU_TRAFFIC_BYTES_DECODE = {
 # ncu capture; a workload is left out until a capture of the kernels as
 # benchmarked exists.
 NCU_TRAFFIC_BYTES_BWD = {
-    "b2h16n4096d128_causal": 438_636_288,
+    "b2h16n4096d128_causal": 437_043_712,
 }
 NCU_TRAFFIC_BYTES = {
     "b2h16n4096d128_causal": 140_705_280,
-    "b2h16n4096d256_causal": 579_028_224,
+    "b2h16n4096d256_causal": 575_434_624,
 }
 
 
