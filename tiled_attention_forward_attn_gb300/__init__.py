@@ -6,6 +6,12 @@ CPU or PyTorch fallback; if the library is missing, every call raises.
 
 Names follow the C ABI: :func:`fa_fwd` takes preallocated device tensors;
 :func:`attention_forward` allocates the outputs and calls :func:`fa_fwd`.
+Also: :func:`fa_fwd_host` (the forward for tensors in host memory, copies
+included), :func:`fa_fwd_splitkv` / :func:`attention_forward_splitkv` (few
+queries against many keys) and :func:`fa_fwd_splitkv_static`,
+:func:`fa_bwd` / :func:`attention_backward` (gradients, bf16 or fp16),
+:func:`attention_forward_order_ablation` (the two loop orders), and the
+device status / test-hook functions.
 """
 from __future__ import annotations
 
