@@ -769,8 +769,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     w = workloads.by_name(args.workload)
     if args.pass_ == "bwd":
-        if not isinstance(w, workloads.Workload) or w.d not in (64, 128):
-            ap.error("--pass bwd takes a square workload with d = 64 or 128")
+        if not isinstance(w, workloads.Workload) or w.d > 128 or w.d % 16:
+            ap.error("--pass bwd takes a square workload with d a multiple of 16 up to 128")
         if args.impl == "reference":
             return run_reference_bwd(args, w)
         return run_ours_bwd(args, w)

@@ -40,7 +40,7 @@ enum fa_status {
   FA_OK = 0,
   FA_ERR_NULL = 1,      /* a required pointer is NULL */
   FA_ERR_SHAPE = 2,     /* B, H or N <= 0, or B*H*N*d overflows the index space */
-  FA_ERR_HEAD_DIM = 3,  /* d is not 64 or 128 */
+  FA_ERR_HEAD_DIM = 3,  /* d is not a head dimension the entry point takes */
   FA_ERR_ALIGN = 4,     /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
   FA_ERR_SCALE = 5,     /* scale is NaN or infinite */
   FA_ERR_ALIAS = 6,     /* o or lse overlaps an input, or o overlaps lse */
@@ -230,7 +230,9 @@ size_t fa_fwd_splitkv_static_scratch_bytes(void);
  *                      q, k, v, causal and scale
  *   lse              : const fp32 [B][H][N] (device, 4-byte aligned)
  *   dq, dk, dv       : bf16 [B][H][N][d] (device), written
- *   d                : 64 or 128;  causal, scale as for fa_fwd
+ *   d                : a multiple of 16 from 16 to 128 (computed in 64- or
+ *                      128-wide tiles whose extra columns are zeros and are
+ *                      never stored);  causal, scale as for fa_fwd
  *   workspace        : device scratch of at least fa_bwd_workspace_bytes()
  *                      bytes (16-byte aligned), owned by the caller,
  *                      overwritten (D and LSE * log2(e) per query row)

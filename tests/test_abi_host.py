@@ -237,9 +237,13 @@ def test_bwd_validation(lib):
 
     # 2 rows of D and LSE*log2(e) per head, padded to 384 rows: 2 * 2 * 384 * 4 bytes
     assert lib.fa_bwd_workspace_bytes(1, 2, 300, 64) == 6144
-    assert lib.fa_bwd_workspace_bytes(1, 2, 300, 96) == 0
+    # head dimensions: multiples of 16 from 16 to 128
+    assert lib.fa_bwd_workspace_bytes(1, 2, 300, 96) == 6144
+    assert lib.fa_bwd_workspace_bytes(1, 2, 300, 16) == 6144
+    for bad in (0, 8, 72, 144, 256):
+        assert lib.fa_bwd_workspace_bytes(1, 2, 300, bad) == 0
+        assert call(d=bad) == FA_ERR_HEAD_DIM
     assert call(q=0) == FA_ERR_NULL
-    assert call(d=96) == FA_ERR_HEAD_DIM
     assert call(N=0) == FA_ERR_SHAPE
     assert call(dk=8 * big + 8) == FA_ERR_ALIGN
     assert call(scale=float("nan")) == FA_ERR_SCALE
@@ -266,7 +270,8 @@ def test_bwd_ex_validation(lib):
     assert call(7) == FA_ERR_DTYPE
     assert call(-1) == FA_ERR_DTYPE
     assert call(1, q=0) == FA_ERR_NULL
-    assert call(1, d=96) == FA_ERR_HEAD_DIM
+    assert call(1, d=72) == FA_ERR_HEAD_DIM
+    assert call(1, d=256) == FA_ERR_HEAD_DIM
     assert call(1, ws_bytes=6000) == FA_ERR_WORKSPACE
     if not torch.cuda.is_available():
         assert call(1) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)

@@ -101,6 +101,47 @@ def test_bwd_more_tiles_than_sms(fa, cuda_device, d, causal):
     check_grads(got, ref, f"H20 N1000 d{d} causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [16, 32, 48, 80, 96, 112])
+@pytest.mark.parametrize("N", [129, 300])
+def test_bwd_other_head_dims(fa, cuda_device, N, d, causal, dtype):
+    """Head dimensions below 64 run in the D = 64 layout, those between 64
+    and 128 in the D = 128 one: the columns past d arrive as zeros (they add
+    nothing to S or dP) and are never stored."""
+    q, k, v = workloads.generate_shape(1, 2, N, d, seed=1800 + N + d, qk_std=1.5, dtype=dtype)
+    do = workloads.generate_shape(1, 2, N, d, seed=1900 + N + d, dtype=dtype)[0]
+    scale = 1.0 / math.sqrt(d)
+    got = _grads(fa, cuda_device, q, k, v, do, causal, scale, dtype=dtype)
+    ref = oracle.attention_bwd(q, k, v, do, causal, scale, dtype=dtype)
+    check_grads(got, ref, f"{dtype} N{N} d{d} c{causal}")
+
+
+@pytest.mark.parametrize("d", [48, 96])
+def test_bwd_narrow_rows_write_nothing_past_d(fa, cuda_device, d):
+    """dQ, dK and dV placed at the very front of larger buffers holding a
+    sentinel: the rows are d wide (not the layout's 64 or 128), so a store
+    past column d of the last row would land in the sentinel."""
+    import torch
+
+    B, H, N = 1, 3, 200
+    q, k, v = workloads.generate_shape(B, H, N, d, seed=2000 + d, qk_std=1.5)
+    do = workloads.generate_shape(B, H, N, d, seed=2100 + d)[0]
+    qd, kd, vd, dod = (workloads.as_torch(a).to(cuda_device) for a in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=True, scale=0.2)
+    n = B * H * N * d
+    bufs = [torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device=cuda_device)
+            for _ in range(3)]
+    dq, dk, dv = (b[:n].view(B, H, N, d) for b in bufs)
+    fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, True, 0.2)
+    torch.cuda.synchronize(cuda_device)
+    assert fa.fa_get_device_status() == 0
+    for b in bufs:
+        assert bool((b[n:] == 7.0).all())
+    got = [t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+    check_grads(got, oracle.attention_bwd(q, k, v, do, True, 0.2), f"sentinel d{d}")
+
+
 def test_bwd_deterministic_and_workspace_checked(fa, cuda_device):
     import torch
 

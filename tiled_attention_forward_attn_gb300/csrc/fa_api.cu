@@ -460,7 +460,7 @@ int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensor
   const int64_t threads = rows * (D / 8);  // a multiple of 256: Npad is a multiple of 128
   fa::fa_bwd_prep_kernel<D, kF16><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
-      const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad);
+      const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad, base.d);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   // Persistent grids: one CTA per SM (at most one per tile) walks the tiles.
   const unsigned ctas = static_cast<unsigned>(
@@ -475,8 +475,13 @@ int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensor
 
 }  // namespace
 
+// Head dimensions of the backward: multiples of 16 up to 128, laid out in the
+// kernels' D = 64 or D = 128 tiles (columns past d arrive as zeros and are
+// never stored).
+bool bwd_head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+
 extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  if (B <= 0 || H <= 0 || N <= 0 || !bwd_head_dim_ok(d)) return 0;
   const int64_t BH = static_cast<int64_t>(B) * H;
   return static_cast<size_t>(2 * BH * bwd_npad(N) * 4);
 }
@@ -496,7 +501,7 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
   if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1)) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  if (!bwd_head_dim_ok(d)) return FA_ERR_HEAD_DIM;
   const int64_t BH = static_cast<int64_t>(B) * H;
   const int64_t Npad = bwd_npad(N);
   const int64_t T = Npad / fa::kBwdTile;
@@ -547,6 +552,7 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   prm.lse2 = ws;
   prm.dvec = ws + BH * Npad;
   prm.N = N;
+  prm.d = d;
   prm.Npad = static_cast<int>(Npad);
   prm.T = static_cast<int>(T);
   prm.num_bh = static_cast<int>(BH);
@@ -559,15 +565,16 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   prm_q.out0 = static_cast<uint16_t*>(dq);
   prm_q.out1 = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool narrow = d <= 64;  // the D = 64 layout
   if (f16)
-    return d == 64 ? launch_bwd<64, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
-                                          prm, prm_q, sms, st)
-                   : launch_bwd<128, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
-                                           prm, prm_q, sms, st);
-  return d == 64 ? launch_bwd<64, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+    return narrow ? launch_bwd<64, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
                                          prm, prm_q, sms, st)
-                 : launch_bwd<128, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                  : launch_bwd<128, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
                                           prm, prm_q, sms, st);
+  return narrow ? launch_bwd<64, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                                        prm, prm_q, sms, st)
+                : launch_bwd<128, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
+                                         prm, prm_q, sms, st);
 }
 
 // ------------------------------------------------------- loop-order ablation

@@ -71,11 +71,12 @@ constexpr int kBwdSub = 64;    // streamed rows per sub-step
 constexpr int kBwdEwCols = kBwdSub / 4;  // columns of a sub-step per elementwise warpgroup
 
 struct BwdParams {
-  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][D] bf16 or fp16
+  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][d] bf16 or fp16
   uint16_t* out1;     // key-tile pass: dV; unused otherwise
   const float* lse2;  // [BH][Npad] -LSE * log2(e) per query (0 past N)
   const float* dvec;  // [BH][Npad] -rowsum(dO * O) per query (0 past N)
   int N;              // sequence length
+  int d;              // head dimension (<= D, a multiple of 16; columns past it are zeros)
   int Npad;           // N rounded up to whole tiles
   int T;              // tiles per (batch, head) = Npad / 128
   int num_bh;         // B * H
@@ -145,7 +146,7 @@ template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ lse2,
-                       float* __restrict__ dvec, int N, int Npad) {
+                       float* __restrict__ dvec, int N, int Npad, int d) {
   constexpr int kTpr = D / 8;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = gid / kTpr;  // padded row index bh * Npad + n
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(256)
   const int64_t bh = row / Npad;
   const int n = static_cast<int>(row - bh * Npad);
   float acc = 0.0f;
-  if (n < N) {
-    const size_t off = (static_cast<size_t>(bh) * N + n) * D + part * 8;
+  if (n < N && part * 8 < d) {
+    const size_t off = (static_cast<size_t>(bh) * N + n) * d + part * 8;
     const uint4 a = *reinterpret_cast<const uint4*>(o + off);
     const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
@@ -398,15 +399,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const bool in_range = x_idx < p.N;
       constexpr int kCols = kKV ? D / 2 : D / 4;
       const int part = kKV ? (g & 1) : g;
       const bool is_dv = kKV && g >= 2;
       const uint32_t col = (is_dv ? C::kColAcc1 : C::kColAcc0) + kCols * part;
       const float mul = is_dv ? 1.0f : p.scale;
       uint16_t* out = is_dv ? p.out1 : p.out0;
-      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * D +
-                                            kCols * part);
       uint32_t racc[kCols];
 #pragma unroll
       for (int cc = 0; cc < kCols / 16; ++cc)
@@ -418,15 +416,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.acc_free());
+      // Packed to 16 bits first: half the registers live across the stores.
+      uint32_t w[kCols / 2];
 #pragma unroll
-      for (int q8 = 0; q8 < kCols / 8; ++q8) {
-        uint32_t w4[4];
+      for (int e = 0; e < kCols / 2; ++e)
+        w[e] = pack_x2<kF16>(__uint_as_float(racc[2 * e]) * mul, __uint_as_float(racc[2 * e + 1]) * mul);
+      // 16-byte groups of this thread's part that exist: none past the last
+      // row, and none past column d (d may be below the layout's D).
+      const int live8 = x_idx < p.N ? (p.d - kCols * part) / 8 : 0;
+      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * p.d +
+                                            kCols * part);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w4[e] = pack_x2<kF16>(__uint_as_float(racc[8 * q8 + 2 * e]) * mul,
-                                __uint_as_float(racc[8 * q8 + 2 * e + 1]) * mul);
-        if (in_range) dst[q8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
+      for (int q8 = 0; q8 < kCols / 8; ++q8)
+        if (q8 < live8) dst[q8] = make_uint4(w[4 * q8], w[4 * q8 + 1], w[4 * q8 + 2], w[4 * q8 + 3]);
     }
   } else if (warp == kBwdLoadWarp) {
     // ------------------------------------------------------------ producer
