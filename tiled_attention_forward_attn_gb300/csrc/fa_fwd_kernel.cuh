@@ -87,7 +87,6 @@ constexpr int kRowThreadsPerTile = 128;
 constexpr int kLoadWarp = 8;  // Q, K and V producer
 constexpr int kMmaWarp = 9;   // warps 10 and 11 only fill the third warpgroup
 constexpr uint32_t kSwBlockBytes = 128 * 128;  // [128 rows x 64 bf16] swizzled block
-constexpr float kRescaleThreshold = 8.0f;      // log2 units: P stays <= 2^8
 // A half tile's P sum above 2^15 moves the reference: at or below it every P
 // is <= 2^15, inside the fp16 range (max 65504) and far inside bf16's.
 constexpr float kPSumLimit = 32768.0f;
