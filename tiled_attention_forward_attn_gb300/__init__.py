@@ -370,7 +370,8 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, worksp
     """Attention backward into preallocated CUDA tensors (C ABI ``fa_bwd_ex``).
 
     q, k, v, o, dout, dq, dk, dv: contiguous ``[B, H, N, d]`` CUDA tensors of one
-    element type, ``torch.bfloat16`` or ``torch.float16``, on one device; lse:
+    element type, ``torch.bfloat16`` or ``torch.float16``, on one device, d a
+    multiple of 16 from 16 to 128; lse:
     ``torch.float32`` ``[B, H, N]`` (o and lse from :func:`fa_fwd`).
     ``workspace``: a CUDA byte tensor of at least :func:`fa_bwd_workspace_bytes`;
     allocated here when None.
