@@ -1,7 +1,9 @@
 // Fused attention forward for head dimension 256 on sm_103a: the method of
-// fa_fwd_kernel.cuh (tiled online softmax, "Q/O stay, K/V move", causal
-// tiles past the diagonal skipped, lazy exponent reference, one division at
-// the end), laid out for a 256-column accumulator.
+// fa_fwd_kernel.cuh (the tiled online softmax of "Parsing FlashAttention (2):
+// FlashAttention-v1 forward pass" §2-§3 in the loop order of "Online Softmax
+// and FlashAttention", course unit 12: "Q/O stay, K/V move", causal tiles
+// past the diagonal skipped, lazy exponent reference, one division at the
+// end), laid out for a 256-column accumulator.
 //
 // Two query tiles per CTA would need 2 x (128 + 256) TMEM columns, more than
 // the 512 there are, so a work unit is one 128-row query tile and the
