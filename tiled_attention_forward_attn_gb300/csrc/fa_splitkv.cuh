@@ -440,7 +440,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int e = 0; e < kCols; ++e) o[e] = fmaf(w, src[e], o[e]);
   }
-  const float inv = 1.0f / total;
+  // total is 0 only when every range timed out (each partial LSE is -inf):
+  // O is then written as zeros, as the clustered merge does.
+  const float inv = total > 0.0f ? 1.0f / total : 0.0f;
   uint16_t* dst = p.o + static_cast<size_t>(row) * D + lane * kCols;
 #pragma unroll
   for (int e = 0; e < kCols; e += 2) {
