@@ -202,8 +202,9 @@ int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_split
  * rejected with FA_ERR_SCRATCH_LIMIT before anything is enqueued.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call on a device shares the one array, which keeps the
+ * device, with that device current, and again after the device's context
+ * has been replaced, e.g. by cudaDeviceReset); make that first call before
+ * any stream capture.  Every call on a device shares the one array, which keeps the
  * last call's contents (nothing in it needs to start at zero); calls whose
  * kernels overlap on the GPU, e.g. on two unordered streams or from two
  * host threads, race on it and give undefined results: order them on one

@@ -839,7 +839,9 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
 // The buffer is a file-scope device array: every GPU that loads this library
 // holds kStaticScratchBytes of it until the process exits.  Its name is only
 // a host-side handle; the device address comes from cudaGetSymbolAddress,
-// taken once per device (with that device current) on the first call there.
+// taken once per device (with that device current) on the first call there,
+// and again whenever that device's current context is a different one (after
+// a cudaDeviceReset the module is loaded anew, possibly at another address).
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
@@ -847,15 +849,48 @@ static __device__ __align__(256) uint8_t g_splitkv_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};  // context id the address belongs to
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void load_ctx_queries() {
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn != nullptr)
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn != nullptr)
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
+// Process-unique id of the current context (never reused for another
+// context), or 0 when it cannot be queried.
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_once, load_ctx_queries);
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 // Device address of the scratch array on `dev` (the current device).
 int static_scratch(int dev, void** out) {
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_scratch_addr[dev] == nullptr || ctx == 0 || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) != cudaSuccess || ptr == nullptr)
       return FA_ERR_LAUNCH;
     g_scratch_addr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return FA_OK;
