@@ -90,29 +90,6 @@ static void score_row_fmt(const uint16_t *q_row, const uint16_t *k, int64_t i,
 }
 
 /*
- * One row of scores (page 1 §1.1; page 2 causal passage):
- *   s_j = scale * sum_t q_t * k_{j,t}     for visible j,
- *   s_j = -inf                           for j > i when causal.
- * q_row: d bf16 values of query i; k: n_keys x d bf16 row-major.
- */
-void oracle_score_row(const uint16_t *q_row, const uint16_t *k, int64_t i,
-                      int64_t n_keys, int64_t d, double scale, int causal,
-                      double *s)
-{
-    for (int64_t j = 0; j < n_keys; ++j) {
-        if (causal && j > i) {
-            s[j] = -INFINITY;
-            continue;
-        }
-        double dot = 0.0;
-        for (int64_t t = 0; t < d; ++t)
-            dot += oracle_bf16_to_double(q_row[t]) *
-                   oracle_bf16_to_double(k[j * d + t]);
-        s[j] = scale * dot;
-    }
-}
-
-/*
  * Safe softmax of one vector (page 1 §2.1, eqs (1)-(5)):
  *   m = max_j x_j,  shifted_j = x_j - m,  f_j = exp(shifted_j),
  *   l = sum_j f_j,  p_j = f_j / l.
@@ -147,8 +124,8 @@ void oracle_scores(const uint16_t *q, const uint16_t *k, int64_t nq,
                    int64_t row_offset, double *s_out)
 {
     for (int64_t r = 0; r < nq; ++r)
-        oracle_score_row(q + r * d, k, row_offset + r, nk, d, scale, causal,
-                         s_out + r * nk);
+        score_row_fmt(q + r * d, k, row_offset + r, nk, d, scale, causal,
+                      ORACLE_BF16, s_out + r * nk);
 }
 
 /*
