@@ -23,7 +23,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -105,73 +104,169 @@ def load_peaks():
 
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+    """Samples the SM clock, the clock-event (throttle) reasons and the power
+    draw of one GPU through NVML's read-only queries (libnvidia-ml, called
+    with ctypes), in a background thread every ~2 ms and on demand
+    (sample()); only samples taken between mark_start() and mark_stop() count.
+    Changes no setting of the GPU."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_CLOCK_SM = 1
+    # nvmlClocksEventReason* bits (NVML API)
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, dev_index: int):
+        self.samples = []  # (perf_counter, sm_mhz, reasons_mask, power_mw)
         self.t_start = self.t_stop = None
+        self.error = None
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._lock = threading.Lock()
+        self.nvml = self.handle = None
+        try:
+            import ctypes
+
+            self.ct = ctypes
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            self.handle = self._find_handle(dev_index)
+            mx = ctypes.c_uint(0)
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM,
+                                                   ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+                or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError) as e:
+            self.error = f"NVML unavailable: {e}"
+            self.nvml = self.handle = None
+
+    def _find_handle(self, dev_index: int):
+        """NVML handle of the CUDA device: by UUID, else by the index that
+        CUDA_VISIBLE_DEVICES maps it to."""
+        import torch
+
+        ct = self.ct
+        handle = ct.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(dev_index), "uuid", None)
+        if uuid is not None:
+            text = str(uuid)
+            if not text.startswith("GPU-"):
+                text = "GPU-" + text
+            if self.nvml.nvmlDeviceGetHandleByUUID(text.encode(), ct.byref(handle)) == 0:
+                return handle
+        index = dev_index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if ids and all(x.isdigit() for x in ids) and dev_index < len(ids):
+            index = int(ids[dev_index])
+        if self.nvml.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(index), ct.byref(handle)) != 0:
+            raise OSError("no NVML handle for the device")
+        return handle
+
+    def sample(self):
+        if self.handle is None:
+            return
+        ct = self.ct
+        mhz, mask, mw = ct.c_uint(0), ct.c_ulonglong(0), ct.c_uint(0)
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ct.byref(mhz)) != 0:
+            return
+        self._reasons_fn(self.handle, ct.byref(mask))
+        self.nvml.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        with self._lock:
+            self.samples.append((time.perf_counter(), float(mhz.value), int(mask.value),
+                                 float(mw.value)))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.sample()
+            self._stop.wait(0.002)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+        if self.handle is None:
             return
-        self._reader = threading.Thread(target=self._read, daemon=True)
-        self._reader.start()
-        time.sleep(0.3)
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
 
     def mark_start(self):
-        self.t_start = time.time()
+        self.t_start = time.perf_counter()
 
     def mark_stop(self):
-        self.t_stop = time.time()
+        self.t_stop = time.perf_counter()
 
     def stop(self):
-        if self.proc is None:
-            return None
-        time.sleep(0.15)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self._reader.join(timeout=2)
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
         return self.summary()
 
     def summary(self):
-        rows = [(t, l.split(", ")) for t, l in self.lines if l]
-        inside = [r for t, r in rows if self.t_start is not None and self.t_start <= t <= self.t_stop]
-        use = inside if inside else rows
-        if not use:
-            return None
-        sm = [float(r[1]) for r in use if len(r) >= 9 and r[1].replace(".", "").isdigit()]
-        sm_max = [float(r[2]) for r in use if len(r) >= 9 and r[2].replace(".", "").isdigit()]
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = set()
-        for r in use:
-            if len(r) < 9:
-                continue
-            for name, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(sm_max) if sm_max else None,
-                "reasons": sorted(reasons),
-                "samples": len(use), "samples_in_timed_region": len(inside)}
+        if self.handle is None:
+            return {"sm_mhz": None, "samples_in_timed_region": 0, "error": self.error}
+        with self._lock:
+            inside = [x for x in self.samples
+                      if self.t_start is not None and self.t_stop is not None
+                      and self.t_start <= x[0] <= self.t_stop]
+        out = {"source": "NVML (read-only queries, ~2 ms period, in process)",
+               "sm_max_mhz": self.max_mhz, "samples_in_timed_region": len(inside)}
+        if not inside:
+            out.update({"sm_mhz": None, "reasons": [],
+                        "note": "no sample fell inside the timed region"})
+            return out
+        mhz = [x[1] for x in inside]
+        reasons = sorted({name for x in inside for name, bit in self.REASONS.items()
+                          if x[2] & bit})
+        out.update({"sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz),
+                    "sm_mhz_max": max(mhz), "reasons": reasons,
+                    "power_w_max": max(x[3] for x in inside) / 1000.0})
+        return out
+
+
+def timed_launches(step, flush, steps: int, warmup: int, stream, dev, world: int, sampler):
+    """Warm-up, then `steps` timed steps, each bracketed by CUDA events on
+    `stream` and followed by an untimed L2 flush; barrier + synchronize on
+    both sides of the timed region.  The clock sampler runs from before the
+    warm-up, and one untimed flush keeps the GPU busy up to the first timed
+    step (as every later step follows a flush), so no timed step starts on an
+    idle GPU.  While the GPU works through the queued steps the host samples
+    the clocks too.  Returns (per-step ms list, clock summary or None)."""
+    import torch
+
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for _ in range(warmup):
+        step()
+        flush()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    flush()
+    for i in range(steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        flush()
+    while not ends[-1].query():
+        if sampler:
+            sampler.sample()
+        time.sleep(0.0005)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_stop()
+    if world > 1:
+        torch.distributed.barrier()
+    per_launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    clocks = sampler.stop() if sampler else None
+    if clocks and clocks.get("sm_mhz"):
+        med = statistics.median(per_launch_ms)
+        clocks["step_kcycles_at_median_mhz"] = med * clocks["sm_mhz"]  # ms x MHz = kcycles
+    return per_launch_ms, clocks
 
 
 def reduce_max_over_ranks(values, device=None):
@@ -374,34 +469,10 @@ def run_ours(args, w):
         def step():
             fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
 
-    for _ in range(args.warmup):
-        step()
-        flush()
-    torch.cuda.synchronize(dev)
-
     sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_start()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-        flush()
-    torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_stop()
-    if world > 1:
-        torch.distributed.barrier()
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_launch_ms, clocks = timed_launches(step, flush, args.steps, args.warmup, stream, dev,
+                                           world, sampler)
     kernel_ms = sum(per_launch_ms)
-    clocks = sampler.stop() if sampler else None
 
     # End to end, every step from pinned host inputs to pinned host outputs.
     # The forward goes through the C ABI's host-buffer entry point
@@ -634,33 +705,10 @@ def run_ours_bwd(args, w):
     def step():
         fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, w.causal, w.scale, ws, stream)
 
-    for _ in range(args.warmup):
-        step()
-        flush()
-    torch.cuda.synchronize(dev)
     sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_start()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-        flush()
-    torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_stop()
-    if world > 1:
-        torch.distributed.barrier()
-    per_launch_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    per_launch_ms, clocks = timed_launches(step, flush, args.steps, args.warmup, stream, dev,
+                                           world, sampler)
     kernel_ms = sum(per_launch_ms)
-    clocks = sampler.stop() if sampler else None
 
     # End to end: Q, K, V, O, LSE, dO in from pinned host memory, dQ, dK, dV out.
     hosts_in = [workloads.as_torch(a, elem).pin_memory() for a in (q, k, v)]
