@@ -302,6 +302,11 @@ const char *fa_strerror(int code);
  * Returns FA_OK or FA_ERR_LAUNCH; *status must not be NULL (FA_ERR_NULL).
  */
 #define FA_DEVICE_STATUS_TIMEOUT 1u
+/* Set only by the guarded build of the library (libfa_guarded.so, the same
+ * sources compiled with FA_GUARDED=1): a TMA tile origin, TMEM column range,
+ * shared-memory destination or global store failed its bounds check; the
+ * access was skipped (outputs undefined, no fault).  Never set by libfa.so. */
+#define FA_DEVICE_STATUS_BOUNDS 2u
 int fa_get_device_status(unsigned int *status);
 int fa_clear_device_status(void);
 

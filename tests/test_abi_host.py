@@ -47,6 +47,16 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, f"declared in include/*.h but not exported: {missing}"
 
 
+def test_guarded_build_exports_every_declared_symbol(lib):
+    """The bounds-checked twin (FA_GUARDED=1) is built beside the library and
+    exports the same C ABI."""
+    from tiled_attention_forward_attn_gb300 import _build
+
+    glib = ctypes.CDLL(_build.GUARDED_LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(glib, n)]
+    assert not missing, f"not exported by the guarded build: {missing}"
+
+
 def test_strerror_and_version(lib):
     for code in range(0, 10):
         assert isinstance(lib.fa_strerror(code), bytes) and lib.fa_strerror(code)

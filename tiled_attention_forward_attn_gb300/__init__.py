@@ -11,7 +11,9 @@ included), :func:`fa_fwd_splitkv` / :func:`attention_forward_splitkv` (few
 queries against many keys) and :func:`fa_fwd_splitkv_static`,
 :func:`fa_bwd` / :func:`attention_backward` (gradients, bf16 or fp16),
 :func:`attention_forward_order_ablation` (the two loop orders), and the
-device status / test-hook functions.
+device status / test-hook functions.  :func:`reload_library` switches to
+another build of the library, e.g. ``GUARDED_LIB_PATH`` (every tile origin,
+TMEM range and store bounds-checked; FA_DEVICE_STATUS_BOUNDS on a failure).
 """
 from __future__ import annotations
 
@@ -29,12 +31,14 @@ __all__ = [
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
     "fa_bwd", "fa_bwd_workspace_bytes", "attention_backward", "attention_forward_order_ablation",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
-    "fa_set_fault_injection", "load_library", "LIB_PATH",
-    "FA_DEVICE_STATUS_TIMEOUT", "FA_INJECT_SKIP_FIRST_V_LOAD",
+    "fa_set_fault_injection", "load_library", "reload_library", "LIB_PATH", "GUARDED_LIB_PATH",
+    "FA_DEVICE_STATUS_TIMEOUT", "FA_DEVICE_STATUS_BOUNDS", "FA_INJECT_SKIP_FIRST_V_LOAD",
 ]
 
 LIB_PATH = _build.LIB_PATH
+GUARDED_LIB_PATH = _build.GUARDED_LIB_PATH
 FA_DEVICE_STATUS_TIMEOUT = 1
+FA_DEVICE_STATUS_BOUNDS = 2
 FA_INJECT_SKIP_FIRST_V_LOAD = 1
 
 _lock = threading.Lock()
@@ -111,6 +115,16 @@ def load_library(path: str | None = None):
         lib.fa_fwd_splitkv_static_scratch_bytes.argtypes = []
         _lib = lib
         return lib
+
+
+def reload_library(path: str | None = None):
+    """Make later calls use the library at `path` (default: LIB_PATH), e.g.
+    GUARDED_LIB_PATH; returns it.  Each build keeps its own device status
+    word."""
+    global _lib
+    with _lock:
+        _lib = None
+    return load_library(path)
 
 
 def fa_strerror(code: int) -> str:

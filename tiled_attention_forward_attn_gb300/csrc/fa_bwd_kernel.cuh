@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(256)
   }
 #pragma unroll
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (part == 0) {
+  if (part == 0 && guard(bh >= 0 && n >= 0 && n < Npad)) {
     dvec[row] = n < N ? -acc : 0.0f;
     lse2[row] = n < N ? -lse[static_cast<size_t>(bh) * N + n] * 1.4426950408889634f : 0.0f;
   }
@@ -423,7 +423,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         w[e] = pack_x2<kF16>(__uint_as_float(racc[2 * e]) * mul, __uint_as_float(racc[2 * e + 1]) * mul);
       // 16-byte groups of this thread's part that exist: none past the last
       // row, and none past column d (d may be below the layout's D).
-      const int live8 = x_idx < p.N ? (p.d - kCols * part) / 8 : 0;
+      const int live8 = (x_idx < p.N && guard(bh < p.num_bh && x_idx >= 0 && p.d <= D))
+                            ? (p.d - kCols * part) / 8
+                            : 0;
       uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * p.d +
                                             kCols * part);
 #pragma unroll
@@ -449,6 +451,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive_expect_tx(bars.x_full(), 2 * C::kTileBytes);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
+          if (!tma_coord_ok(64 * b, p.d, u.xt * kBwdTile, p.N, u.bh, p.num_bh) ||
+              !smem_range_ok(C::kOffX + C::kTileBytes + b * kSwBlockBytes, kSwBlockBytes, C::kOffY))
+            continue;
           tma_load_3d_hint(sX + b * kSwBlockBytes, &tm_x0, bars.x_full(), 64 * b,
                            u.xt * kBwdTile, u.bh, once);
           tma_load_3d_hint(sX + C::kTileBytes + b * kSwBlockBytes, &tm_x1, bars.x_full(), 64 * b,
@@ -470,12 +475,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive_expect_tx(bars.y_full(s), C::kStageBytes + C::kVecBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b) {
+            // A streamed half may start past N (the last tile's second half
+            // when N is ragged): TMA reads it as zeros; it must start inside
+            // the padded extent.
+            if (!tma_coord_ok(64 * b, p.d, row0, p.Npad, u.bh, p.num_bh) ||
+                !smem_range_ok(C::kOffY + s * C::kStageBytes + C::kHalfBytes + b * C::kHalfBlock,
+                               C::kHalfBlock, C::kOffVec))
+              continue;
             tma_load_3d_hint(stage + b * C::kHalfBlock, &tm_y0, bars.y_full(s), 64 * b, row0, u.bh,
                              keep);
             tma_load_3d_hint(stage + C::kHalfBytes + b * C::kHalfBlock, &tm_y1, bars.y_full(s),
                              64 * b, row0, u.bh, keep);
           }
-          if (kKV) {
+          if (kKV && guard(row0 >= 0 && row0 + kBwdSub <= p.Npad && u.bh < p.num_bh) &&
+              smem_range_ok(C::kOffVec + s * C::kVecBytes, C::kVecBytes, C::kOffBar)) {
             const size_t v0 = static_cast<size_t>(u.bh) * p.Npad + row0;
             const uint32_t vec = sbase + C::kOffVec + s * C::kVecBytes;
             bulk_load(vec, p.lse2 + v0, kBwdSub * 4, bars.y_full(s));
@@ -525,7 +538,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t y0 = yk_lo + (st >> 4);
       const uint32_t y1 = yk_lo + ((st + C::kHalfBytes) >> 4);
       constexpr uint32_t x1 = C::kTileBytes >> 4;
-      if (leader) {
+      if (leader && tmem_range_ok(tmem + C::kColS + kBwdSub * b, kBwdSub) &&
+          tmem_range_ok(tmem + C::kColDP + kBwdSub * b, kBwdSub) &&
+          (kKV || tmem_range_ok(tmem + C::kColXT, D)) && guard(stage < static_cast<uint32_t>(S))) {
         if (kKV) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
@@ -555,7 +570,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // buffer b.  `first`: the tile's first sub-step overwrites the accumulators.
     auto issue_acc = [&](int b, uint32_t stage, bool first) {
       const uint32_t st = stage * C::kStageBytes;
-      if (leader) {
+      if (leader && tmem_range_ok(tmem + C::kColAcc0, D) &&
+          (!kKV || tmem_range_ok(tmem + C::kColAcc1, D)) &&
+          tmem_range_ok(tmem + C::kColS + kBwdSub * b, kBwdSub) &&
+          tmem_range_ok(tmem + C::kColDP + kBwdSub * b, kBwdSub) &&
+          guard(stage < static_cast<uint32_t>(S))) {
 #pragma unroll
         for (int kk = 0; kk < kBwdSub / 16; ++kk) {
           const uint32_t acc = (!first || kk > 0) ? 1u : 0u;

@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kW_Threads, 1)
           fmul2(a0, a1, __uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1]), inv_l, inv_l);
           w[i] = pack_x2<kF16>(a0, a1);
         }
-        if (in_range) {
+        if (in_range && guard(u.bh < p.num_bh && u.h < p.H && q_idx >= 0)) {
           if (p.o_vec32) {
 #pragma unroll
             for (int g = 0; g < 8; ++g) st_global_v8(orow + 128 * hh + 16 * g, &w[8 * g]);
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kW_Threads, 1)
           }
         }
       }
-      if (in_range)
+      if (in_range && guard(u.bh < p.num_bh && q_idx >= 0))
         p.lse[static_cast<size_t>(u.bh) * p.N + q_idx] = (m_ref + __log2f(l_run)) * 0.6931471805599453f;
       // O is read: the next unit's first P.V (which overwrites O) waits for
       // that unit's first p_full, after this point.
@@ -380,8 +380,11 @@ __global__ void __launch_bounds__(kW_Threads, 1)
           mbar_arrive_expect_tx(bars.kv_full(s), C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < kW_D / 64; ++b)
-            tma_load_4d_hint(sRing + s * C::kKVBytes + b * C::kKVBlock, map, bars.kv_full(s),
-                             64 * b, row0, cur_h, cur_b, keep);
+            if (tma_coord_ok(64 * b, kW_D, row0, p.N, cur_b * p.H + cur_h, p.num_bh) &&
+                smem_range_ok(C::kOffRing + s * C::kKVBytes + b * C::kKVBlock, C::kKVBlock,
+                              C::kOffBar))
+              tma_load_4d_hint(sRing + s * C::kKVBytes + b * C::kKVBlock, map, bars.kv_full(s),
+                               64 * b, row0, cur_h, cur_b, keep);
         }
         ++ic;
         return true;
@@ -398,7 +401,9 @@ __global__ void __launch_bounds__(kW_Threads, 1)
         mbar_arrive_expect_tx(bars.q_full(), C::kQBytes);
 #pragma unroll
         for (int b = 0; b < kW_D / 64; ++b)
-          tma_load_4d_hint(sQ + b * C::kQBlock, &tm_q, bars.q_full(), 64 * b, u.q0, u.h, u.b, once);
+          if (tma_coord_ok(64 * b, kW_D, u.q0, p.N, u.bh, p.num_bh) &&
+              smem_range_ok(C::kOffQ + b * C::kQBlock, C::kQBlock, C::kOffRing))
+            tma_load_4d_hint(sQ + b * C::kQBlock, &tm_q, bars.q_full(), 64 * b, u.q0, u.h, u.b, once);
         ++qc;
         // Items in the order the MMAs read them: K_0, K_1, then V_j, K_j+2.
         bool ok = issue(&tm_k, 0, false) && (u.n < 2 || issue(&tm_k, kW_BlockN, false));
@@ -439,7 +444,8 @@ __global__ void __launch_bounds__(kW_Threads, 1)
     // the K tile in ring slot `slot`.
     auto issue_s = [&](int b, uint32_t slot) {
       const uint32_t kb = k_lo + ((slot * C::kKVBytes) >> 4);
-      if (leader) {
+      if (leader && tmem_range_ok(tmem + C::kColS + 64u * b, kW_BlockN) &&
+          tmem_range_ok(tmem + C::kColQ, kW_D / 2) && guard(slot < static_cast<uint32_t>(R))) {
 #pragma unroll
         for (int kk = 0; kk < kW_D / 16; ++kk)
           umma_ts_lohi(tmem + C::kColS + 64u * b, tmem + C::kColQ + 8u * kk,
@@ -450,7 +456,9 @@ __global__ void __launch_bounds__(kW_Threads, 1)
     };
     auto issue_pv = [&](int b, uint32_t slot, bool first) {  // O (+)= P_b V, 4 slices of 16 keys
       const uint32_t vb = v_lo + ((slot * C::kKVBytes) >> 4);
-      if (leader) {
+      if (leader && tmem_range_ok(tmem + C::kColO, kW_D) &&
+          tmem_range_ok(tmem + C::kColS + 64u * b, kW_BlockN / 2) &&
+          guard(slot < static_cast<uint32_t>(R))) {
 #pragma unroll
         for (int kk = 0; kk < kW_BlockN / 16; ++kk)
           umma_ts_lohi(tmem + C::kColO, tmem + C::kColS + 64u * b + 8u * kk,

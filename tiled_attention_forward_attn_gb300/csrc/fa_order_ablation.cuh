@@ -80,12 +80,14 @@ __device__ __forceinline__ bool ord_wait(uint32_t bar, uint32_t parity, uint64_t
 }
 
 // Loads a 64-row tile (rows r0.., slice bh) of a [BH][N][D] tensor.
+// rows, nbh: the tensor's row count and slice count (for the guarded build).
 template <int D>
 __device__ __forceinline__ void ord_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, int r0,
-                                         int bh) {
+                                         int bh, int rows, int nbh) {
 #pragma unroll
   for (int b = 0; b < D / 64; ++b)
-    tma_load_3d(dst + b * kOrdTile * 128, map, bar, 64 * b, r0, bh);
+    if (tma_coord_ok(64 * b, D, r0, rows, bh, nbh))
+      tma_load_3d(dst + b * kOrdTile * 128, map, bar, 64 * b, r0, bh);
 }
 
 // S = Q K^T for this warp's 16 query rows against the 64 keys of a tile,
@@ -213,11 +215,11 @@ __global__ void __launch_bounds__(kOrdThreads)
     auto kv_stage = [&](int s) { return sbase + C::kOffKV + s * 2 * C::kTileBytes; };
     if (threadIdx.x == 0) {
       expect(0, C::kTileBytes);
-      ord_load<D>(sQ, &tm_q, bar0, q0, bh);
+      ord_load<D>(sQ, &tm_q, bar0, q0, bh, p.N, p.num_bh);
       for (int j = 0; j < 2 && j < nj; ++j) {
         expect(1 + j, 2 * C::kTileBytes);
-        ord_load<D>(kv_stage(j), &tm_k, bar0 + 8 * (1 + j), j * kOrdTile, bh);
-        ord_load<D>(kv_stage(j) + C::kTileBytes, &tm_v, bar0 + 8 * (1 + j), j * kOrdTile, bh);
+        ord_load<D>(kv_stage(j), &tm_k, bar0 + 8 * (1 + j), j * kOrdTile, bh, p.N, p.num_bh);
+        ord_load<D>(kv_stage(j) + C::kTileBytes, &tm_v, bar0 + 8 * (1 + j), j * kOrdTile, bh, p.N, p.num_bh);
       }
     }
     bool ok = __syncthreads_and(wait(0));
@@ -267,8 +269,8 @@ __global__ void __launch_bounds__(kOrdThreads)
       __syncthreads();  // every warp is done with stage s
       if (threadIdx.x == 0 && j + 2 < nj) {
         expect(1 + s, 2 * C::kTileBytes);
-        ord_load<D>(sK, &tm_k, bar0 + 8 * (1 + s), (j + 2) * kOrdTile, bh);
-        ord_load<D>(sV, &tm_v, bar0 + 8 * (1 + s), (j + 2) * kOrdTile, bh);
+        ord_load<D>(sK, &tm_k, bar0 + 8 * (1 + s), (j + 2) * kOrdTile, bh, p.N, p.num_bh);
+        ord_load<D>(sV, &tm_v, bar0 + 8 * (1 + s), (j + 2) * kOrdTile, bh, p.N, p.num_bh);
       }
     }
     if (!ok) {
@@ -286,10 +288,10 @@ __global__ void __launch_bounds__(kOrdThreads)
 #pragma unroll
     for (int n = 0; n < kN; ++n) {
       const int col = 8 * n + 2 * t4;
-      if (r0 < p.N)
+      if (r0 < p.N && guard(bh < p.num_bh && col + 2 <= D))
         *reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bh) * p.N + r0) * D + col) =
             pack_bf16x2(acc[n][0] * i0, acc[n][1] * i0);
-      if (r1 < p.N)
+      if (r1 < p.N && guard(bh < p.num_bh && col + 2 <= D))
         *reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bh) * p.N + r1) * D + col) =
             pack_bf16x2(acc[n][2] * i1, acc[n][3] * i1);
     }
@@ -313,11 +315,11 @@ __global__ void __launch_bounds__(kOrdThreads)
     const int ni = p.T - i_first;
     if (threadIdx.x == 0) {
       expect(0, 2 * C::kTileBytes);
-      ord_load<D>(sK, &tm_k, bar0, j * kOrdTile, bh);
-      ord_load<D>(sV, &tm_v, bar0, j * kOrdTile, bh);
+      ord_load<D>(sK, &tm_k, bar0, j * kOrdTile, bh, p.N, p.num_bh);
+      ord_load<D>(sV, &tm_v, bar0, j * kOrdTile, bh, p.N, p.num_bh);
       const uint32_t s = q_loads & 1u;
       expect(1 + s, C::kTileBytes);
-      ord_load<D>(q_stage(s), &tm_q, bar0 + 8 * (1 + s), i_first * kOrdTile, bh);
+      ord_load<D>(q_stage(s), &tm_q, bar0 + 8 * (1 + s), i_first * kOrdTile, bh, p.N, p.num_bh);
     }
     ok = __syncthreads_and(wait(0));
     for (int ii = 0; ok && ii < ni; ++ii) {
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kOrdThreads)
       const uint32_t s = (q_loads + ii) & 1u;
       if (threadIdx.x == 0 && ii + 1 < ni) {  // prefetch the next Q tile
         expect(1 + (s ^ 1u), C::kTileBytes);
-        ord_load<D>(q_stage(s ^ 1u), &tm_q, bar0 + 8 * (1 + (s ^ 1u)), (i + 1) * kOrdTile, bh);
+        ord_load<D>(q_stage(s ^ 1u), &tm_q, bar0 + 8 * (1 + (s ^ 1u)), (i + 1) * kOrdTile, bh, p.N, p.num_bh);
       }
       ok = __syncthreads_and(wait(1 + s));
       if (!ok) break;
@@ -390,13 +392,13 @@ __global__ void __launch_bounds__(kOrdThreads)
         o1.x = o1.x * c10 + pv[n][2] * c11;
         o1.y = o1.y * c10 + pv[n][3] * c11;
         if (last) {
-          if (r0 < p.N)
+          if (r0 < p.N && guard(bh < p.num_bh && col + 2 <= D))
             *reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bh) * p.N + r0) * D + col) =
                 pack_bf16x2(o0.x, o0.y);
-          if (r1 < p.N)
+          if (r1 < p.N && guard(bh < p.num_bh && col + 2 <= D))
             *reinterpret_cast<uint32_t*>(p.o + (static_cast<size_t>(bh) * p.N + r1) * D + col) =
                 pack_bf16x2(o1.x, o1.y);
-        } else {
+        } else if (guard(bh < p.num_bh && r1 < p.Npad && col + 2 <= D)) {
           *reinterpret_cast<float2*>(p.ws_o + w0 * D + col) = o0;
           *reinterpret_cast<float2*>(p.ws_o + w1 * D + col) = o1;
         }
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kOrdThreads)
         if (last) {
           if (r0 < p.N) p.lse[static_cast<size_t>(bh) * p.N + r0] = (mn0 + __log2f(ln0)) * 0.6931471805599453f;
           if (r1 < p.N) p.lse[static_cast<size_t>(bh) * p.N + r1] = (mn1 + __log2f(ln1)) * 0.6931471805599453f;
-        } else {
+        } else if (guard(bh < p.num_bh && r1 < p.Npad)) {
           p.ws_m[w0] = mn0;
           p.ws_m[w1] = mn1;
           p.ws_l[w0] = ln0;

@@ -191,6 +191,10 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
           mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b) {
+            if (!tma_coord_ok(64 * b, D, k0, p.Nk, bh, p.num_bh) ||
+                !smem_range_ok(s * C::kStageBytes + C::kTileBytes + b * C::kBoxBytes, C::kBoxBytes,
+                               C::kOffBar))
+              continue;
             tma_load_3d_hint(stage + b * C::kBoxBytes, &tm_k, bar_full + 8 * s, 64 * b, k0, bh,
                              policy);
             tma_load_3d_hint(stage + C::kTileBytes + b * C::kBoxBytes, &tm_v, bar_full + 8 * s,
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
     if (kCluster) {
       part_o[i * D + col] = o;
       if (col == 0) part_lse[i] = lse;
-    } else {
+    } else if (guard(split < p.splits && bh < p.num_bh && i < Nq && col < D)) {
       p.ws_o[(row_base + i) * D + col] = o;
       if (col == 0) p.ws_lse[row_base + i] = lse;
     }
@@ -407,8 +411,10 @@ __global__ void __launch_bounds__(kSplitThreads, kSplitCtasPerSm)
       }
       const size_t orow = static_cast<size_t>(bh) * Nq + i;
       const float inv = total > 0.0f ? 1.0f / total : 0.0f;
-      reinterpret_cast<__nv_bfloat16*>(p.o)[orow * D + col] = __float2bfloat16_rn(o * inv);
-      if (col == 0) p.lse[orow] = m + __logf(total);
+      if (guard(bh < p.num_bh && i < Nq && col < D)) {
+        reinterpret_cast<__nv_bfloat16*>(p.o)[orow * D + col] = __float2bfloat16_rn(o * inv);
+        if (col == 0) p.lse[orow] = m + __logf(total);
+      }
     }
     cluster_sync_all();  // the other CTAs' partials stay alive until here
   }
@@ -444,6 +450,7 @@ __global__ void __launch_bounds__(256)
   // O is then written as zeros, as the clustered merge does.
   const float inv = total > 0.0f ? 1.0f / total : 0.0f;
   uint16_t* dst = p.o + static_cast<size_t>(row) * D + lane * kCols;
+  if (!guard(row < p.num_bh * p.Nq && lane * kCols + kCols <= D)) return;
 #pragma unroll
   for (int e = 0; e < kCols; e += 2) {
     const uint32_t pk = pack_bf16x2(o[e] * inv, o[e + 1] * inv);

@@ -11,6 +11,92 @@
 namespace fa {
 
 // ----------------------------------------------------------------------------
+// Device status word and the guarded build
+// ----------------------------------------------------------------------------
+// Sticky bit set read by fa_get_device_status (FA_DEVICE_STATUS_* values).
+__device__ uint32_t g_fa_status;
+constexpr uint32_t kStatusTimeout = 1u;  // a bounded wait ran out
+constexpr uint32_t kStatusBounds = 2u;   // guarded build: an access failed its bounds check
+
+// The guarded build (compiled with -DFA_GUARDED=1 into its own library)
+// checks every TMA tile coordinate, TMEM column range and global store
+// against its bounds before the access; a failed check sets kStatusBounds and
+// the access is skipped (a skipped copy then ends in a timed-out wait, a
+// skipped store leaves memory untouched), so nothing faults.  In the normal
+// build every check is the constant true and compiles away.
+#ifndef FA_GUARDED
+#define FA_GUARDED 0
+#endif
+constexpr uint32_t kTmemMaxCols = 512;  // every kernel allocates all 512 columns
+
+__device__ __forceinline__ bool guard(bool ok) {
+#if FA_GUARDED
+  if (!ok) atomicOr(&g_fa_status, kStatusBounds);
+  return ok;
+#else
+  (void)ok;
+  return true;
+#endif
+}
+
+// A warp-wide TMEM access of `ncols` columns at taddr (lane in bits 31-16,
+// column in bits 15-0): the columns lie inside the allocation and the lane
+// base is the calling warp's quarter (warp % 4) of the 128 lanes.
+__device__ __forceinline__ bool tmem_cols_ok(uint32_t taddr, uint32_t ncols) {
+#if FA_GUARDED
+  const uint32_t col = taddr & 0xFFFFu, lane = taddr >> 16;
+  return guard(col + ncols <= kTmemMaxCols && lane == 32u * ((threadIdx.x >> 5) & 3u));
+#else
+  (void)taddr;
+  (void)ncols;
+  return true;
+#endif
+}
+
+// An MMA operand or accumulator of `ncols` TMEM columns at taddr (any lane
+// base is the MMA's own: only the column range is checked).
+__device__ __forceinline__ bool tmem_range_ok(uint32_t taddr, uint32_t ncols) {
+#if FA_GUARDED
+  return guard((taddr & 0xFFFFu) + ncols <= kTmemMaxCols && (taddr >> 16) == 0u);
+#else
+  (void)taddr;
+  (void)ncols;
+  return true;
+#endif
+}
+
+// [off, off + bytes) inside a shared-memory region of `size` bytes.
+__device__ __forceinline__ bool smem_range_ok(uint32_t off, uint32_t bytes, uint32_t size) {
+#if FA_GUARDED
+  return guard(off <= size && bytes <= size - off);
+#else
+  (void)off;
+  (void)bytes;
+  (void)size;
+  return true;
+#endif
+}
+
+// A TMA tile origin: column x a non-negative multiple of 8 elements (16
+// bytes) below the head dimension, row in [0, rows), and the index of the
+// outer dimension(s) in [0, outer).
+__device__ __forceinline__ bool tma_coord_ok(int x, int d, int row, int rows, int outer_idx,
+                                             int outer) {
+#if FA_GUARDED
+  return guard(x >= 0 && (x & 7) == 0 && x < d && row >= 0 && row < rows && outer_idx >= 0 &&
+               outer_idx < outer);
+#else
+  (void)x;
+  (void)d;
+  (void)row;
+  (void)rows;
+  (void)outer_idx;
+  (void)outer;
+  return true;
+#endif
+}
+
+// ----------------------------------------------------------------------------
 // Generic helpers
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -252,6 +338,10 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uin
 // Thread t of warp w reads/writes TMEM lane 32*(w%4)+t, columns [col, col+32).
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  if (!tmem_cols_ok(taddr, 32)) {
+    for (int i = 0; i < 32; ++i) r[i] = 0u;
+    return;
+  }
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -265,6 +355,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  if (!tmem_cols_ok(taddr, 32)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
@@ -279,6 +370,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  if (!tmem_cols_ok(taddr, 16)) {
+    for (int i = 0; i < 16; ++i) r[i] = 0u;
+    return;
+  }
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -297,6 +392,7 @@ __device__ __forceinline__ void tmem_ld_fence16(uint32_t (&r)[16]) {
 }
 
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  if (!tmem_cols_ok(taddr, 8)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
