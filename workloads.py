@@ -65,14 +65,17 @@ WORKLOADS = (
 HEADLINE = WORKLOADS[2]
 
 # The headline shape in fp16, at head dimension 96 (a multiple of 16 below
-# the 128-column layout) and at head dimension 256: the element-type and
-# head-dimension variants of the forward.
+# the 128-column layout), at head dimension 256 and at head dimension 64 (the
+# 64-column layout): the element-type and head-dimension variants of the
+# forward.
 VARIANT_WORKLOADS = (
     Workload("b2h16n4096d128_causal_fp16", 2, 16, 4096, 128, True, 1.0 / math.sqrt(128), seed=7,
              rows="sampled", dtype="f16"),
     Workload("b2h16n4096d96_causal", 2, 16, 4096, 96, True, 1.0 / math.sqrt(96), seed=8,
              rows="sampled"),
     Workload("b2h16n4096d256_causal", 2, 16, 4096, 256, True, 1.0 / 16.0, seed=9,
+             rows="sampled"),
+    Workload("b2h16n4096d64_causal", 2, 16, 4096, 64, True, 1.0 / 8.0, seed=10,
              rows="sampled"),
 )
 
