@@ -485,13 +485,20 @@ def run_ours(args, w):
     hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
-    host_path = not decode and not args.loop_order
+    host_path = not args.loop_order
     streams = [stream, torch.cuda.Stream(dev)]
-    if host_path:
+    if host_path and decode:
+        ws_host = [torch.empty(fa.fa_fwd_splitkv_host_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, 0),
+                               dtype=torch.uint8, device=dev) for _ in range(2)]
+    elif host_path:
         ws_host = [torch.empty(fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d),
                                dtype=torch.uint8, device=dev) for _ in range(2)]
 
     def e2e_step(i):
+        if host_path and decode:
+            fa.fa_fwd_splitkv_host(hq, hk, hv, ho[i % 2], hl[i % 2], w.causal, w.scale, 0,
+                                   ws_host[i % 2], streams[i % 2])
+            return
         if host_path:
             fa.fa_fwd_host(hq, hk, hv, ho[i % 2], hl[i % 2], w.causal, w.scale, ws_host[i % 2],
                            streams[i % 2])
@@ -552,7 +559,9 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": DECODE_UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "ms_per_step": e2e_ms / e2e_steps},
+                    "ms_per_step": e2e_ms / e2e_steps,
+                    "path": "fa_fwd_splitkv_host (C ABI, host buffers), steps alternating "
+                            "between two streams"},
             # one clustered launch per step when the ranges fit in a cluster
             # (<= 8), else the split pass and the combine pass
             "gpu_launches": (1 if n_splits <= 8 else 2) * args.steps,
@@ -714,27 +723,32 @@ def run_ours_bwd(args, w):
     hosts_in = [workloads.as_torch(a, elem).pin_memory() for a in (q, k, v)]
     hosts_in += [o.cpu().pin_memory(), lse.cpu().pin_memory(),
                  workloads.as_torch(do, elem).pin_memory()]
-    devs_in = [qd, kd, vd, o, lse, dod]
     hosts_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hosts_in)
     d2h = sum(t.numel() * t.element_size() for t in hosts_out)
 
-    def e2e_step():
-        for dst, src in zip(devs_in, hosts_in):
-            dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in zip(hosts_out, (dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
+    # Every step through the C ABI's host-buffer entry point (fa_bwd_host: six
+    # uploads, the three backward launches, three downloads on one stream),
+    # steps alternating between two streams with their own device staging.
+    outs2 = [hosts_out, [torch.empty_like(t).pin_memory() for t in hosts_out]]
+    streams = [stream, torch.cuda.Stream(dev)]
+    ws_host = [torch.empty(fa.fa_bwd_host_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                           device=dev) for _ in range(2)]
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_step(i):
+        fa.fa_bwd_host(*hosts_in, *outs2[i % 2], w.causal, w.scale, ws_host[i % 2], streams[i % 2])
+
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     e2e_steps = max(10, min(args.steps, 100))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     kernel_ms, e2e_ms = reduce_max_over_ranks([kernel_ms, e2e_ms], device=dev)
@@ -779,7 +793,9 @@ def run_ours_bwd(args, w):
             "cpu_baseline": cpu,
             "e2e": {"value": job_tflops(world, flops_step, e2e_steps, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "ms_per_step": e2e_ms / e2e_steps},
+                    "ms_per_step": e2e_ms / e2e_steps,
+                    "path": "fa_bwd_host (C ABI, host buffers), steps alternating between two "
+                            "streams"},
             "gpu_launches": 3 * args.steps,
             "launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
                           "max": max(per_launch_ms)},

@@ -181,6 +181,34 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n
 int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
 
 /*
+ * fa_fwd_splitkv_host — fa_fwd_splitkv for inputs and outputs in HOST memory:
+ * on `stream` it queues the copies of q, k, v into the caller's device
+ * workspace (one cudaMemcpyAsync each), the split-KV launch(es), and the
+ * copies of O and LSE back.  The pages' method has no counterpart; it is the
+ * end-to-end path of a decode caller whose tensors live on the host.
+ *
+ *   q_host, k_host, v_host, o_host, lse_host : as fa_fwd_splitkv's device
+ *       tensors (bf16 [B][H][Nq|Nk][d], fp32 [B][H][Nq]), contiguous, host
+ *   B .. num_splits : as for fa_fwd_splitkv
+ *   workspace : device memory of at least fa_fwd_splitkv_host_workspace_bytes()
+ *       bytes, 256-byte aligned, owned by the caller (Q, K, V, O, LSE and the
+ *       split partials staged there, overwritten)
+ * Host outputs must not overlap a host input or each other (FA_ERR_ALIAS).
+ * Everything fa_fwd_splitkv would reject is rejected before any copy is
+ * queued; FA_ERR_WORKSPACE when the workspace is missing or small.  The host
+ * outputs hold the result once `stream` has been synchronised; the host
+ * inputs must stay unchanged until then.
+ */
+int fa_fwd_splitkv_host(const void *q_host, const void *k_host, const void *v_host, void *o_host,
+                        float *lse_host, int B, int H, int Nq, int Nk, int d, int causal,
+                        float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/* Device workspace bytes fa_fwd_splitkv_host needs on the current device (0
+ * on invalid arguments or without a usable device when num_splits == 0). */
+size_t fa_fwd_splitkv_host_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * fa_fwd_splitkv_static — fa_fwd_splitkv for callers that cannot allocate
  * device memory.  The pages have no counterpart: this is a library service.
  *
@@ -262,6 +290,35 @@ int fa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const 
 
 /* Workspace bytes fa_bwd and fa_bwd_ex need (0 on invalid arguments). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_bwd_host — fa_bwd_ex for inputs and outputs in HOST memory: on `stream`
+ * it queues the copies of q, k, v, o, lse and dout into the caller's device
+ * workspace (one cudaMemcpyAsync each), the three backward launches, and the
+ * copies of dq, dk, dv back.  The pages' method has no counterpart; it is
+ * the end-to-end path of a caller whose tensors live on the host.
+ *
+ *   q_host .. dout_host : as fa_bwd_ex's device inputs (`dtype` [B][H][N][d],
+ *                         fp32 lse [B][H][N]), contiguous, host
+ *   dq_host, dk_host, dv_host : `dtype` [B][H][N][d], host, written
+ *   dtype .. scale      : as for fa_bwd_ex
+ *   workspace           : device memory of at least fa_bwd_host_workspace_bytes()
+ *                         bytes, 256-byte aligned, owned by the caller (the
+ *                         nine tensors and the backward's workspace staged
+ *                         there, overwritten)
+ * Host outputs must not overlap a host input or each other (FA_ERR_ALIAS).
+ * Everything fa_bwd_ex would reject is rejected before any copy is queued;
+ * FA_ERR_WORKSPACE when the workspace is missing or small.  The host outputs
+ * hold the result once `stream` has been synchronised; the host inputs must
+ * stay unchanged until then.
+ */
+int fa_bwd_host(const void *q_host, const void *k_host, const void *v_host, const void *o_host,
+                const float *lse_host, const void *dout_host, void *dq_host, void *dk_host,
+                void *dv_host, int dtype, int B, int H, int N, int d, int causal, float scale,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Device workspace bytes fa_bwd_host needs (0 on invalid arguments). */
+size_t fa_bwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * fa_fwd_order_ablation — the attention forward of fa_fwd in one of the two

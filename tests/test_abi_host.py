@@ -314,3 +314,60 @@ def test_fwd_host_validation(lib):
     assert call(lse=4 * big + 256) == FA_ERR_ALIAS   # LSE inside O
     if not torch.cuda.is_available():
         assert call() in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_splitkv_host_validation(lib):
+    """fa_fwd_splitkv_host rejects bad arguments before queueing any copy."""
+    import torch
+
+    big = 1 << 24
+    # With num_splits > 0 the sizes need no device.
+    part = lib.fa_fwd_splitkv_workspace_bytes(1, 2, 5, 1000, 64, 4)
+    need = lib.fa_fwd_splitkv_host_workspace_bytes(1, 2, 5, 1000, 64, 4)
+    assert part > 0
+    assert need == (2 * _r256(2 * 5 * 64 * 2) + 2 * _r256(2 * 1000 * 64 * 2) + _r256(2 * 5 * 4)
+                    + _r256(part))
+    assert lib.fa_fwd_splitkv_host_workspace_bytes(1, 2, 5, 1000, 96, 4) == 0
+
+    def call(q=big, Nq=5, d=64, causal=1, scale=0.1):
+        return lib.fa_fwd_splitkv_host(q, 2 * big, 3 * big, 4 * big, 5 * big, 1, 2, Nq, 1000, d,
+                                       causal, scale, 4, 1 << 30, 1 << 26, None)
+
+    assert call(q=0) == FA_ERR_NULL
+    assert call(Nq=17) == FA_ERR_SHAPE
+    assert call(d=96) == FA_ERR_HEAD_DIM
+    assert call(causal=2) == FA_ERR_SHAPE
+    assert call(scale=float("inf")) == FA_ERR_SCALE
+    if not torch.cuda.is_available():
+        assert call() in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
+def test_bwd_host_validation(lib):
+    """fa_bwd_host rejects bad arguments before queueing any copy."""
+    import torch
+
+    big = 1 << 24
+    need = lib.fa_bwd_host_workspace_bytes(1, 2, 300, 64)
+    ws_bwd = lib.fa_bwd_workspace_bytes(1, 2, 300, 64)
+    assert ws_bwd == 2 * 2 * 384 * 4
+    assert need == 8 * _r256(2 * 300 * 64 * 2) + _r256(2 * 300 * 4) + _r256(ws_bwd)
+    assert lib.fa_bwd_host_workspace_bytes(1, 2, 300, 72) == 0
+
+    def call(q=big, dq=7 * big, dtype=0, d=64, causal=1, ws=1 << 30, ws_bytes=1 << 24):
+        return lib.fa_bwd_host(q, 2 * big, 3 * big, 4 * big, 5 * big, 6 * big, dq, 8 * big,
+                               9 * big, dtype, 1, 2, 300, d, causal, 0.1, ws, ws_bytes, None)
+
+    assert call(q=0) == FA_ERR_NULL
+    assert call(dtype=4) == 12  # FA_ERR_DTYPE
+    assert call(d=72) == FA_ERR_HEAD_DIM
+    assert call(causal=2) == FA_ERR_SHAPE
+    assert call(ws_bytes=need - 1) == 10  # FA_ERR_WORKSPACE
+    assert call(ws=(1 << 30) + 16) == FA_ERR_ALIGN
+    assert call(dq=big + 128) == FA_ERR_ALIAS  # dQ over Q
+    if not torch.cuda.is_available():
+        assert call() in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+

@@ -10,6 +10,7 @@ Also: :func:`fa_fwd_host` (the forward for tensors in host memory, copies
 included), :func:`fa_fwd_splitkv` / :func:`attention_forward_splitkv` (few
 queries against many keys) and :func:`fa_fwd_splitkv_static`,
 :func:`fa_bwd` / :func:`attention_backward` (gradients, bf16 or fp16),
+:func:`fa_fwd_splitkv_host` and :func:`fa_bwd_host` (host tensors, copies included),
 :func:`attention_forward_order_ablation` (the two loop orders), and the
 device status / test-hook functions.  :func:`reload_library` switches to
 another build of the library, e.g. ``GUARDED_LIB_PATH`` (every tile origin,
@@ -29,7 +30,9 @@ __all__ = [
     "fa_fwd_host", "fa_fwd_host_workspace_bytes",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
-    "fa_bwd", "fa_bwd_workspace_bytes", "attention_backward", "attention_forward_order_ablation",
+    "fa_fwd_splitkv_host", "fa_fwd_splitkv_host_workspace_bytes",
+    "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_host", "fa_bwd_host_workspace_bytes",
+    "attention_backward", "attention_forward_order_ablation",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
     "fa_set_fault_injection", "load_library", "reload_library", "LIB_PATH", "GUARDED_LIB_PATH",
     "FA_DEVICE_STATUS_TIMEOUT", "FA_DEVICE_STATUS_BOUNDS", "FA_INJECT_SKIP_FIRST_V_LOAD",
@@ -113,6 +116,16 @@ def load_library(path: str | None = None):
         lib.fa_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_splitkv_static_scratch_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_splitkv_static_scratch_bytes.argtypes = []
+        lib.fa_fwd_splitkv_host.restype = i
+        lib.fa_fwd_splitkv_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp,
+                                            ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_splitkv_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.fa_bwd_host.restype = i
+        lib.fa_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp,
+                                    ctypes.c_size_t, vp]
+        lib.fa_bwd_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_bwd_host_workspace_bytes.argtypes = [i, i, i, i]
         _lib = lib
         return lib
 
@@ -257,6 +270,89 @@ def fa_fwd_host(q, k, v, o, lse, causal: bool, scale: float, workspace, stream=N
             B, H, N, d, int(bool(causal)), float(scale), workspace.data_ptr(),
             workspace.numel(), handle or None)
         _check(rc, "fa_fwd_host")
+
+
+def _host_stream(workspace, stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_host(name, t, dt, shape):
+    if tuple(t.shape) != tuple(shape) or t.dtype != dt or t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of shape {tuple(shape)}")
+
+
+def fa_fwd_splitkv_host_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int,
+                                        num_splits: int = 0) -> int:
+    """Device workspace bytes fa_fwd_splitkv_host needs on the current device."""
+    return int(load_library().fa_fwd_splitkv_host_workspace_bytes(B, H, Nq, Nk, d, num_splits))
+
+
+def fa_fwd_splitkv_host(q, k, v, o, lse, causal: bool, scale: float, num_splits: int, workspace,
+                        stream=None) -> None:
+    """Split-KV forward with host tensors (C ABI ``fa_fwd_splitkv_host``):
+    copies Q, K, V into ``workspace``, runs the split-KV path and copies O
+    and LSE back, all queued on ``stream``; synchronise before reading.
+
+    q, o: contiguous CPU bf16 ``[B, H, Nq, d]``; k, v: ``[B, H, Nk, d]``;
+    lse: CPU float32 ``[B, H, Nq]``; workspace: a CUDA uint8 tensor of at
+    least :func:`fa_fwd_splitkv_host_workspace_bytes` bytes."""
+    import torch
+
+    B, H, Nq, d = _dims(q)
+    Nk = int(k.shape[2])
+    for name, t, dt, shape in (("q", q, torch.bfloat16, (B, H, Nq, d)),
+                               ("k", k, torch.bfloat16, (B, H, Nk, d)),
+                               ("v", v, torch.bfloat16, (B, H, Nk, d)),
+                               ("o", o, torch.bfloat16, (B, H, Nq, d)),
+                               ("lse", lse, torch.float32, (B, H, Nq))):
+        _check_host(name, t, dt, shape)
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    with torch.cuda.device(workspace.device):
+        rc = load_library().fa_fwd_splitkv_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
+            d, int(bool(causal)), float(scale), int(num_splits), workspace.data_ptr(),
+            workspace.numel(), _host_stream(workspace, stream) or None)
+        _check(rc, "fa_fwd_splitkv_host")
+
+
+def fa_bwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Device workspace bytes fa_bwd_host needs (0 on invalid arguments)."""
+    return int(load_library().fa_bwd_host_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd_host(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, workspace,
+                stream=None) -> None:
+    """Backward with host tensors (C ABI ``fa_bwd_host``): copies Q, K, V, O,
+    LSE, dO into ``workspace``, runs the backward and copies dQ, dK, dV
+    back, all queued on ``stream``; synchronise before reading.
+
+    q, k, v, o, dout, dq, dk, dv: contiguous CPU tensors ``[B, H, N, d]`` of
+    one type (bf16 or fp16); lse: CPU float32 ``[B, H, N]``; workspace: a CUDA
+    uint8 tensor of at least :func:`fa_bwd_host_workspace_bytes` bytes."""
+    import torch
+
+    B, H, N, d = _dims(q)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q must be torch.bfloat16 or torch.float16")
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
+                    ("dv", dv), ("q", q)):
+        _check_host(name, t, q.dtype, (B, H, N, d))
+    _check_host("lse", lse, torch.float32, (B, H, N))
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    with torch.cuda.device(workspace.device):
+        dtype = FA_DTYPE_FP16 if q.dtype == torch.float16 else FA_DTYPE_BF16
+        rc = load_library().fa_bwd_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dtype, B, H, N, d,
+            int(bool(causal)), float(scale), workspace.data_ptr(), workspace.numel(),
+            _host_stream(workspace, stream) or None)
+        _check(rc, "fa_bwd_host")
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

@@ -577,6 +577,83 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
                                          prm, prm_q, sms, st);
 }
 
+// ---------------------------------------------------------------- host buffers (backward)
+// Device staging of fa_bwd_host: Q, K, V, O, dO, dQ, dK, dV, LSE and the
+// backward's workspace, each 256-byte aligned, in that order.
+extern "C" size_t fa_bwd_host_workspace_bytes(int B, int H, int N, int d) {
+  const size_t part = fa_bwd_workspace_bytes(B, H, N, d);
+  if (part == 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return 8 * round256(rows * d * 2) + round256(rows * 4) + round256(part);
+}
+
+extern "C" int fa_bwd_host(const void* q_host, const void* k_host, const void* v_host,
+                           const void* o_host, const float* lse_host, const void* dout_host,
+                           void* dq_host, void* dk_host, void* dv_host, int dtype, int B, int H,
+                           int N, int d, int causal, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  // Everything fa_bwd_ex would reject is rejected here, before any copy is queued.
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host || !dout_host || !dq_host ||
+      !dk_host || !dv_host)
+    return FA_ERR_NULL;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
+  if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1)) return FA_ERR_SHAPE;
+  if (!bwd_head_dim_ok(d)) return FA_ERR_HEAD_DIM;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t Npad = bwd_npad(N);
+  if (BH > INT_MAX || BH * (Npad / fa::kBwdTile) > INT_MAX || BH * Npad > INT_MAX)
+    return FA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  const size_t need = fa_bwd_host_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  const size_t tb = static_cast<size_t>(BH) * N * d * 2;
+  const size_t lb = static_cast<size_t>(BH) * N * 4;
+  // Host outputs overlap neither a host input nor each other.
+  const void* ins[6] = {q_host, k_host, v_host, o_host, lse_host, dout_host};
+  const size_t in_bytes[6] = {tb, tb, tb, tb, lb, tb};
+  const void* outs[3] = {dq_host, dk_host, dv_host};
+  for (int a = 0; a < 3; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], tb, ins[b], in_bytes[b])) return FA_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlaps(outs[a], tb, outs[b], tb)) return FA_ERR_ALIAS;
+  }
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
+  if (prep != FA_OK) return prep;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t t = round256(tb);
+  void* qd = ws;
+  void* kd = ws + t;
+  void* vd = ws + 2 * t;
+  void* od = ws + 3 * t;
+  void* dod = ws + 4 * t;
+  void* dqd = ws + 5 * t;
+  void* dkd = ws + 6 * t;
+  void* dvd = ws + 7 * t;
+  float* ld = reinterpret_cast<float*>(ws + 8 * t);
+  uint8_t* part = ws + 8 * t + round256(lb);
+  const size_t part_bytes = need - static_cast<size_t>(part - ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(qd, q_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(kd, k_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(vd, v_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(od, o_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(ld, lse_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dod, dout_host, tb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const int rc = fa_bwd_ex(qd, kd, vd, od, ld, dod, dqd, dkd, dvd, dtype, B, H, N, d, causal,
+                           scale, part, part_bytes, stream);
+  if (rc != FA_OK) return rc;
+  if (cudaMemcpyAsync(dq_host, dqd, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(dk_host, dkd, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(dv_host, dvd, tb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
 // ------------------------------------------------------- loop-order ablation
 
 namespace {
@@ -826,6 +903,66 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
   prm.inject = g_inject.load(std::memory_order_relaxed);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return d == 64 ? launch_split<64>(mk, mv, prm, s, true) : launch_split<128>(mk, mv, prm, s, true);
+}
+
+
+// ---------------------------------------------------------------- host buffers (split-KV)
+// Device staging of fa_fwd_splitkv_host: Q, K, V, O, LSE and the split
+// partials, each 256-byte aligned, in that order.
+extern "C" size_t fa_fwd_splitkv_host_workspace_bytes(int B, int H, int Nq, int Nk, int d,
+                                                      int num_splits) {
+  const size_t part = fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits);
+  if (part == 0) return 0;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t qb = BH * Nq * d * 2, kvb = BH * Nk * d * 2, lb = BH * Nq * 4;
+  return 2 * round256(qb) + 2 * round256(kvb) + round256(lb) + round256(part);
+}
+
+extern "C" int fa_fwd_splitkv_host(const void* q_host, const void* k_host, const void* v_host,
+                                   void* o_host, float* lse_host, int B, int H, int Nq, int Nk,
+                                   int d, int causal, float scale, int num_splits, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  // Everything fa_fwd_splitkv would reject is rejected here, before any copy is queued.
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host) return FA_ERR_NULL;
+  const int shape = split_shape_ok(B, H, Nq, Nk, d, causal, num_splits);
+  if (shape != FA_OK) return shape;
+  if (!std::isfinite(scale)) return FA_ERR_SCALE;
+  int dev = 0, sms = 0;
+  const int prep = prepare_device(&dev, &sms);
+  if (prep != FA_OK) return prep;
+  const size_t need = fa_fwd_splitkv_host_workspace_bytes(B, H, Nq, Nk, d, num_splits);
+  if (need == 0) return FA_ERR_LAUNCH;
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t qb = BH * Nq * d * 2, kvb = BH * Nk * d * 2, lb = BH * Nq * 4;
+  const void* hin[3] = {q_host, k_host, v_host};
+  const size_t hin_bytes[3] = {qb, kvb, kvb};
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(o_host, qb, hin[i], hin_bytes[i]) || overlaps(lse_host, lb, hin[i], hin_bytes[i]))
+      return FA_ERR_ALIAS;
+  if (overlaps(o_host, qb, lse_host, lb)) return FA_ERR_ALIAS;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qd = ws;
+  void* kd = ws + round256(qb);
+  void* vd = static_cast<uint8_t*>(kd) + round256(kvb);
+  void* od = static_cast<uint8_t*>(vd) + round256(kvb);
+  float* ld = reinterpret_cast<float*>(static_cast<uint8_t*>(od) + round256(qb));
+  uint8_t* part = reinterpret_cast<uint8_t*>(ld) + round256(lb);
+  const size_t part_bytes = need - static_cast<size_t>(part - ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(qd, q_host, qb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(kd, k_host, kvb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(vd, v_host, kvb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const int rc = fa_fwd_splitkv(qd, kd, vd, od, ld, B, H, Nq, Nk, d, causal, scale, num_splits,
+                                part, part_bytes, stream);
+  if (rc != FA_OK) return rc;
+  if (cudaMemcpyAsync(o_host, od, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(lse_host, ld, lb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return FA_OK;
 }
 
 // ----------------------------------------------------------------------------
