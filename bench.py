@@ -78,15 +78,14 @@ NCU_TRAFFIC_BYTES_DECODE = {
     "decode_b4h16q16k16384d128_causal": 538_642_816,
     "decode_b4h16q1k16384d128": 538_550_528,
 }
-# Per-launch DRAM traffic of the forward kernel per workload, from an ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
-# out until a capture of the kernel as benchmarked exists.
 # DRAM bytes (read + write) of one backward step (three launches), from an
 # ncu capture; a workload is left out until a capture of the kernels as
 # benchmarked exists.
 NCU_TRAFFIC_BYTES_BWD = {
-    "b2h16n4096d128_causal": 438_838_272,
 }
+# Per-launch DRAM traffic of the forward kernel per workload, from an ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
+# out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
     "b2h16n4096d128_causal": 136_679_936,
     "b2h16n4096d256_causal": 575_434_624,

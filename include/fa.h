@@ -288,7 +288,38 @@ int fa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const 
               int d, int causal, float scale, void *workspace, size_t workspace_bytes,
               void *stream);
 
-/* Workspace bytes fa_bwd and fa_bwd_ex need (0 on invalid arguments). */
+/*
+ * fa_bwd_strided — fa_bwd_ex with every [B][H][N][d] tensor at its own
+ * strides, as fa_fwd_strided takes them ("pwwt.cn FlashAttention/Triton
+ * walkthrough" §3.4 passes every tensor with its batch, head and row strides).
+ *
+ *   q, k, v, o, dout    : const [B][H][N][d] `dtype` tensors (device, base
+ *                         16-byte aligned); element (b, h, n, c) of tensor X
+ *                         lives at X + b*X_strides[0] + h*X_strides[1] +
+ *                         n*X_strides[2] + c
+ *   dq, dk, dv          : [B][H][N][d] `dtype` tensors (device, base 16-byte
+ *                         aligned), written at their strides
+ *   *_strides           : 3 int64 element strides (batch, head, row), each a
+ *                         non-negative multiple of 8 below 2^38; NULL =
+ *                         contiguous.  Columns are always contiguous.
+ *                         Distinct elements of dq, dk or dv must not overlap
+ *                         (FA_ERR_STRIDE); inputs may share elements.
+ *   lse, workspace, dtype, B .. scale, stream : as for fa_bwd_ex
+ * The address span of each output (first to one past the last element) and
+ * the workspace must overlap no input's span and no other output's
+ * (FA_ERR_ALIAS).  fa_bwd_ex is this call with every stride NULL.  Returns
+ * FA_OK or an FA_ERR_* code; validates before enqueueing; asynchronous.
+ */
+int fa_bwd_strided(const void *q, const int64_t *q_strides, const void *k,
+                   const int64_t *k_strides, const void *v, const int64_t *v_strides,
+                   const void *o, const int64_t *o_strides, const float *lse, const void *dout,
+                   const int64_t *dout_strides, void *dq, const int64_t *dq_strides, void *dk,
+                   const int64_t *dk_strides, void *dv, const int64_t *dv_strides, int dtype,
+                   int B, int H, int N, int d, int causal, float scale, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/* Workspace bytes fa_bwd, fa_bwd_ex and fa_bwd_strided need (0 on invalid
+ * arguments). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*

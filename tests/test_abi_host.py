@@ -288,6 +288,54 @@ def test_bwd_ex_validation(lib):
         assert call(0) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
 
 
+def test_bwd_strided_validation(lib):
+    """fa_bwd_strided: strides are checked like fa_fwd_strided's (non-negative
+    multiples of 8 below 2^38), the gradients' elements must not overlap, and
+    the aliasing check uses each tensor's strided span."""
+    import torch
+
+    big = 1 << 24
+    B, H, N, d = 2, 3, 100, 64
+
+    def call(strides=None, ptrs=None, dtype=0):
+        st = list(strides or [None] * 8)
+        arr = [None if x is None else (ctypes.c_int64 * 3)(*x) for x in st]
+        p = list(ptrs or [big * (i + 1) for i in range(8)])
+        return lib.fa_bwd_strided(p[0], arr[0], p[1], arr[1], p[2], arr[2], p[3], arr[3],
+                                  9 * big, p[4], arr[4], p[5], arr[5], p[6], arr[6], p[7], arr[7],
+                                  dtype, B, H, N, d, 1, 0.1, 10 * big, 1 << 20, None)
+
+    def one(i, st):
+        s = [None] * 8
+        s[i] = st
+        return s
+
+    bnhd = (N * H * d, d, H * d)  # [B, N, H, d] memory viewed as [B, H, N, d]
+    assert call(dtype=2) == FA_ERR_DTYPE
+    for i in range(8):
+        assert call(one(i, (-64, 64, 64))) == FA_ERR_STRIDE, i
+        assert call(one(i, (19200, 6400, 68))) == FA_ERR_STRIDE, i
+        assert call(one(i, (1 << 38, 64, 64))) == FA_ERR_STRIDE, i
+    # overlapping gradient rows or heads; the same strides on an input are allowed
+    for i in (5, 6, 7):
+        assert call(one(i, (19200, 6400, 32))) == FA_ERR_STRIDE, i
+        assert call(one(i, (19200, 64, 64))) == FA_ERR_STRIDE, i
+    # dq starting 4 KiB below k: its strided span reaches into k
+    ptrs = [big * (i + 1) for i in range(8)]
+    ptrs[5] = 2 * big - 4096
+    assert call(one(5, bnhd), ptrs) == FA_ERR_ALIAS
+    # dk, dv interleaved within one [B, N, 2, H, d] buffer: distinct
+    # elements but overlapping spans, rejected as aliasing
+    ptrs = [big * (i + 1) for i in range(8)]
+    ptrs[7] = ptrs[6] + H * d * 2
+    s = [None] * 8
+    s[6] = s[7] = (N * 2 * H * d, d, 2 * H * d)
+    assert call(s, ptrs) == FA_ERR_ALIAS
+    if not torch.cuda.is_available():
+        for st in ([bnhd] * 8, one(1, (6400, 0, 64)), [None] * 8):
+            assert call(st) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
 def test_fwd_host_validation(lib):
     """fa_fwd_host rejects bad arguments before queueing any copy (no GPU
     needed for these checks)."""

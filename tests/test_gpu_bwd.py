@@ -274,3 +274,67 @@ def test_bwd_large_score_range(fa, cuda_device, N, d, causal, dtype):
     ref = oracle.attention_bwd(q, k, v, do, causal, scale, dtype=dtype)
     sigma = bwd_rounding_sigma(q, k, v, do, causal, scale, dtype=dtype)
     check_grads_model(got, ref, sigma, f"qk3 {dtype} N{N} d{d} c{causal}")
+
+
+def _bnhd(t):
+    """t's values in [B, N, H, d] memory, viewed as [B, H, N, d]."""
+    return t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("N,d", [(333, 64), (200, 128), (129, 96)])
+def test_bwd_strided_equals_contiguous(fa, cuda_device, N, d, dtype):
+    """Every tensor in [B, N, H, d] memory, and the gradients in row-padded
+    buffers: the same kernels on the same values, so the gradients equal the
+    contiguous call's bit for bit (and match the oracle); the padding between
+    rows stays untouched."""
+    import torch
+
+    B, H = 2, 3
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = workloads.generate_shape(B, H, N, d, seed=5100 + N + d, qk_std=1.5, dtype=dtype)
+    do = workloads.generate_shape(B, H, N, d, seed=5200 + N + d, dtype=dtype)[0]
+    qd, kd, vd, dod = (workloads.as_torch(a, dtype).to(cuda_device) for a in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=True, scale=scale)
+    ref_grads = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=True, scale=scale)
+
+    qs, ks, vs, os_, dos = (_bnhd(t) for t in (qd, kd, vd, o, dod))
+    assert not qs.is_contiguous() and qs.stride(2) == H * d
+    pads = [torch.full((B, H, N, d + 24), 5.0, dtype=qd.dtype, device=cuda_device)
+            for _ in range(3)]
+    grads = [pb[..., :d] for pb in pads]
+    fa.fa_bwd(qs, ks, vs, os_, lse, dos, *grads, True, scale)
+    torch.cuda.synchronize(cuda_device)
+    assert fa.fa_get_device_status() == 0
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, ref_grads):
+        assert torch.equal(g, r), name
+    for pb in pads:
+        assert bool((pb[..., d:] == 5.0).all())
+    got = [t.float().cpu().numpy().astype(np.float64) for t in grads]
+    check_grads(got, oracle.attention_bwd(q, k, v, do, True, scale, dtype=dtype),
+                f"strided N{N} d{d} {dtype}")
+
+
+def test_bwd_strided_shared_kv_head(fa, cuda_device):
+    """K and V shared by every query head (head stride 0): each head's dK and
+    dV are that head's own share, equal bit for bit to the call with K and V
+    copied into every head."""
+    import torch
+
+    B, H, N, d = 2, 4, 257, 128
+    q, _, _ = workloads.generate_shape(B, H, N, d, seed=5300, qk_std=1.5)
+    _, k1, v1 = workloads.generate_shape(B, 1, N, d, seed=5301, qk_std=1.5)
+    do = workloads.generate_shape(B, H, N, d, seed=5302)[0]
+    qd, dod = (workloads.as_torch(a).to(cuda_device) for a in (q, do))
+    k1d, v1d = (workloads.as_torch(a).to(cuda_device) for a in (k1, v1))
+    ke, ve = k1d.expand(B, H, N, d), v1d.expand(B, H, N, d)
+    assert ke.stride(1) == 0
+    kc, vc = ke.contiguous(), ve.contiguous()
+    o, lse = fa.attention_forward(qd, kc, vc, causal=False, scale=0.1)
+    want = fa.attention_backward(qd, kc, vc, o, lse, dod, causal=False, scale=0.1)
+    got = [torch.empty_like(qd) for _ in range(3)]
+    fa.fa_bwd(qd, ke, ve, o, lse, dod, *got, False, 0.1)
+    torch.cuda.synchronize(cuda_device)
+    assert fa.fa_get_device_status() == 0
+    for name, g, w in zip(("dQ", "dK", "dV"), got, want):
+        assert torch.equal(g, w), name

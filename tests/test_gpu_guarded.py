@@ -110,6 +110,30 @@ def test_guarded_backward(fa, cuda_device, N, d, causal):
     _status_clean(fa)
 
 
+def test_guarded_backward_strided(fa, cuda_device):
+    """Every backward tensor in [B, N, H, d] memory, gradients included."""
+    import torch
+
+    B, H, N, d = 2, 3, 300, 64
+    q, k, v = workloads.generate_shape(B, H, N, d, seed=3650, qk_std=1.5)
+    do = workloads.generate_shape(B, H, N, d, seed=3651)[0]
+    qd, kd, vd, dod = (to_device(a, cuda_device) for a in (q, k, v, do))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=True, scale=0.125)
+
+    def bnhd(t):
+        return t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+
+    grads = [torch.empty((B, N, H, d), dtype=torch.bfloat16, device=cuda_device).permute(
+        0, 2, 1, 3) for _ in range(3)]
+    fa.fa_bwd(bnhd(qd), bnhd(kd), bnhd(vd), bnhd(o), lse, bnhd(dod), *grads, True, 0.125)
+    torch.cuda.synchronize(cuda_device)
+    ref = oracle.attention_bwd(q, k, v, do, True, 0.125)
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, ref):
+        err = np.abs(g.float().cpu().numpy().astype(np.float64) - r) / (1.0 + np.abs(r))
+        assert float(err.max()) <= 3e-2, f"guarded strided backward {name}: {float(err.max()):.3e}"
+    _status_clean(fa)
+
+
 @pytest.mark.parametrize("order", [1, 2])
 def test_guarded_loop_order_ablation(fa, cuda_device, order):
     q, k, v = workloads.generate_shape(1, 2, 300, 64, seed=3700, qk_std=1.5)

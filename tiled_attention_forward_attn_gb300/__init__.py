@@ -27,6 +27,7 @@ from . import _build
 
 __all__ = [
     "FAError", "fa_fwd", "attention_forward", "fa_strerror", "fa_version", "fa_fwd_strided",
+    "fa_bwd_strided",
     "fa_fwd_host", "fa_fwd_host_workspace_bytes",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_num_splits",
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
@@ -105,6 +106,10 @@ def load_library(path: str | None = None):
         lib.fa_bwd_ex.restype = i
         lib.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp,
                                   ctypes.c_size_t, vp]
+        lib.fa_bwd_strided.restype = i
+        lib.fa_bwd_strided.argtypes = [vp, i64p, vp, i64p, vp, i64p, vp, i64p, vp, vp, i64p, vp,
+                                       i64p, vp, i64p, vp, i64p, i, i, i, i, i, i, f, vp,
+                                       ctypes.c_size_t, vp]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_fwd_order_ablation.restype = i
@@ -475,14 +480,35 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
 
 
+def _arr3(st):
+    return None if st is None else (ctypes.c_int64 * 3)(*[int(x) for x in st])
+
+
+def fa_bwd_strided(ptrs, strides, lse_ptr: int, dtype: int, B: int, H: int, N: int, d: int,
+                   causal: bool, scale: float, workspace_ptr: int, workspace_bytes: int,
+                   stream: int = 0) -> int:
+    """Direct call of the strided backward entry point.
+
+    ``ptrs``: device addresses of (q, k, v, o, dout, dq, dk, dv); ``strides``:
+    eight 3-tuples of element strides (batch, head, row) or None, in the same
+    order.  Returns the C return code."""
+    q, k, v, o, do, dq, dk, dv = (int(x) for x in ptrs)
+    sq, sk, sv, so, sdo, sdq, sdk, sdv = (_arr3(x) for x in strides)
+    return int(load_library().fa_bwd_strided(
+        q, sq, k, sk, v, sv, o, so, lse_ptr, do, sdo, dq, sdq, dk, sdk, dv, sdv, int(dtype),
+        int(B), int(H), int(N), int(d), int(bool(causal)), float(scale), workspace_ptr,
+        int(workspace_bytes), stream or None))
+
+
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, workspace=None,
            stream=None) -> None:
-    """Attention backward into preallocated CUDA tensors (C ABI ``fa_bwd_ex``).
+    """Attention backward into preallocated CUDA tensors (C ABI ``fa_bwd_strided``).
 
-    q, k, v, o, dout, dq, dk, dv: contiguous ``[B, H, N, d]`` CUDA tensors of one
-    element type, ``torch.bfloat16`` or ``torch.float16``, on one device, d a
-    multiple of 16 from 16 to 128; lse:
-    ``torch.float32`` ``[B, H, N]`` (o and lse from :func:`fa_fwd`).
+    q, k, v, o, dout, dq, dk, dv: ``[B, H, N, d]`` CUDA tensors of one element
+    type, ``torch.bfloat16`` or ``torch.float16``, on one device, any strides
+    with the last dimension contiguous (strides multiples of 8 elements), d a
+    multiple of 16 from 16 to 128; lse: contiguous ``torch.float32``
+    ``[B, H, N]`` (o and lse from :func:`fa_fwd`).
     ``workspace``: a CUDA byte tensor of at least :func:`fa_bwd_workspace_bytes`;
     allocated here when None.
     """
@@ -492,17 +518,25 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, worksp
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise ValueError("q must be torch.bfloat16 or torch.float16")
     elem = q.dtype
-    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
-                    ("dv", dv)):
+    tensors = (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk),
+               ("dv", dv))
+    for name, t in tensors[1:]:
         if tuple(t.shape) != (B, H, N, d):
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(B, H, N, d)}")
     if tuple(lse.shape) != (B, H, N):
         raise ValueError(f"lse has shape {tuple(lse.shape)}, expected {(B, H, N)}")
-    for name, t, dt in (("q", q, elem), ("k", k, elem), ("v", v, elem), ("o", o, elem),
-                        ("dout", dout, elem), ("dq", dq, elem), ("dk", dk, elem),
-                        ("dv", dv, elem), ("lse", lse, torch.float32)):
-        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.device != q.device:
-            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor on q's device")
+    for name, t in tensors:
+        if t.dtype != elem or not t.is_cuda or t.device != q.device:
+            raise ValueError(f"{name} must be a {elem} CUDA tensor on q's device")
+        if t.stride(3) != 1:
+            raise ValueError(f"{name} must have a contiguous last dimension")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or \
+            lse.device != q.device:
+        raise ValueError("lse must be a contiguous torch.float32 CUDA tensor on q's device")
+
+    def st(t):  # a dimension of extent 1 is never stepped: its stride is irrelevant
+        return tuple(0 if t.shape[i] == 1 else t.stride(i) for i in range(3))
+
     with torch.cuda.device(q.device):
         if workspace is None:
             nbytes = fa_bwd_workspace_bytes(B, H, N, d)
@@ -513,12 +547,11 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, worksp
             stream = torch.cuda.current_stream(q.device)
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         dtype = FA_DTYPE_FP16 if elem == torch.float16 else FA_DTYPE_BF16
-        rc = load_library().fa_bwd_ex(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dtype, B, H, N, d,
-            int(bool(causal)), float(scale), workspace.data_ptr(),
-            workspace.numel() * workspace.element_size(), handle or None)
-        _check(rc, "fa_bwd_ex")
+        rc = fa_bwd_strided([t.data_ptr() for _, t in tensors], [st(t) for _, t in tensors],
+                            lse.data_ptr(), dtype, B, H, N, d, causal, scale,
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            handle)
+        _check(rc, "fa_bwd_strided")
 
 
 def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,

@@ -450,17 +450,28 @@ int64_t bwd_npad(int N) { return (static_cast<int64_t>(N) + fa::kBwdTile - 1) / 
 // Three launches on one stream: D and LSE*log2(e) into the workspace, the
 // dK/dV pass (prm_kv: out0 = dK, out1 = dV), the dQ pass (prm_q: out0 = dQ).
 // mX: 128-row boxes (stationary tiles); mX64: 64-row boxes (streamed halves).
+// Inputs of the D pre-pass: O and dO at their element strides
+// (batch, head, row), and the forward's LSE.
+struct BwdPrepIn {
+  const void* o;
+  const int64_t* os;
+  const void* dout;
+  const int64_t* dos;
+  const float* lse;
+};
+
 template <int D, bool kF16>
-int launch_bwd(const void* o, const void* dout, const float* lse, const CUtensorMap& mq,
-               const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-               const CUtensorMap& mq64, const CUtensorMap& mk64, const CUtensorMap& mv64,
-               const CUtensorMap& mdo64, const fa::BwdParams& base, const fa::BwdParams& prm_q,
-               int sms, cudaStream_t stream) {
+int launch_bwd(const BwdPrepIn& in, const CUtensorMap& mq, const CUtensorMap& mk,
+               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mq64,
+               const CUtensorMap& mk64, const CUtensorMap& mv64, const CUtensorMap& mdo64,
+               const fa::BwdParams& base, const fa::BwdParams& prm_q, int sms,
+               cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(base.num_bh) * base.Npad;
   const int64_t threads = rows * (D / 8);  // a multiple of 256: Npad is a multiple of 128
   fa::fa_bwd_prep_kernel<D, kF16><<<static_cast<unsigned>(threads / 256), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
-      const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad, base.d);
+      static_cast<const uint16_t*>(in.o), static_cast<const uint16_t*>(in.dout), in.lse,
+      const_cast<float*>(base.lse2), const_cast<float*>(base.dvec), base.N, base.Npad, base.d,
+      base.H, in.os[0], in.os[1], in.os[2], in.dos[0], in.dos[1], in.dos[2]);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   // Persistent grids: one CTA per SM (at most one per tile) walks the tiles.
   const unsigned ctas = static_cast<unsigned>(
@@ -494,10 +505,14 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
                    workspace, workspace_bytes, stream);
 }
 
-extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
-                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                         int dtype, int B, int H, int N, int d, int causal, float scale,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+int bwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* ks_in,
+             const void* v, const int64_t* vs_in, const void* o, const int64_t* os_in,
+             const float* lse, const void* dout, const int64_t* dos_in, void* dq,
+             const int64_t* dqs_in, void* dk, const int64_t* dks_in, void* dv,
+             const int64_t* dvs_in, int dtype, int B, int H, int N, int d, int causal,
+             float scale, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_DTYPE;
   if (B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1)) return FA_ERR_SHAPE;
@@ -506,21 +521,36 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   const int64_t Npad = bwd_npad(N);
   const int64_t T = Npad / fa::kBwdTile;
   if (BH > INT_MAX || BH * T > INT_MAX || BH * Npad > INT_MAX) return FA_ERR_SHAPE;
+  const int64_t contig[3] = {static_cast<int64_t>(H) * N * d, static_cast<int64_t>(N) * d, d};
+  // Order: q, k, v, o, dout, dq, dk, dv.
+  const int64_t* st[8] = {qs_in, ks_in, vs_in, os_in, dos_in, dqs_in, dks_in, dvs_in};
+  for (auto& s : st) {
+    if (!s) s = contig;
+    // Multiples of 8 elements keep every row (and every 8-column group the
+    // D pre-pass and the gradient stores move as one 16-byte word) aligned.
+    for (int i = 0; i < 3; ++i)
+      if (s[i] < 0 || s[i] % 8 != 0 || s[i] >= (int64_t(1) << 38)) return FA_ERR_STRIDE;
+  }
+  for (int i = 5; i < 8; ++i)
+    if (!strides_disjoint(B, H, N, d, st[i])) return FA_ERR_STRIDE;
   for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(dq),
                           static_cast<const void*>(dk), static_cast<const void*>(dv),
                           static_cast<const void*>(workspace)})
     if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
   if (!std::isfinite(scale)) return FA_ERR_SCALE;
-  const size_t tb = static_cast<size_t>(BH) * N * d * 2;
   const size_t lb = static_cast<size_t>(BH) * N * 4;
   const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
-  // Outputs (dq, dk, dv, workspace) overlap neither an input nor each other.
+  // Outputs (dq, dk, dv, workspace) overlap neither an input nor each other
+  // (address spans, first to one past the last element).
   const void* ins[6] = {q, k, v, o, lse, dout};
-  const size_t in_bytes[6] = {tb, tb, tb, tb, lb, tb};
+  const size_t in_bytes[6] = {span_bytes(B, H, N, d, st[0]), span_bytes(B, H, N, d, st[1]),
+                              span_bytes(B, H, N, d, st[2]), span_bytes(B, H, N, d, st[3]), lb,
+                              span_bytes(B, H, N, d, st[4])};
   const void* outs[4] = {dq, dk, dv, workspace};
-  const size_t out_bytes[4] = {tb, tb, tb, need};
+  const size_t out_bytes[4] = {span_bytes(B, H, N, d, st[5]), span_bytes(B, H, N, d, st[6]),
+                               span_bytes(B, H, N, d, st[7]), need};
   for (int a = 0; a < 4; ++a) {
     for (int b = 0; b < 6; ++b)
       if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA_ERR_ALIAS;
@@ -534,20 +564,29 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   std::call_once(g_encode_once, load_encode);
   if (g_encode == nullptr) return FA_ERR_LAUNCH;
   CUtensorMap mq, mk, mv, mdo, mq64, mk64, mv64, mdo64;
-  const int bhi = static_cast<int>(BH);
   const bool f16 = dtype == FA_DTYPE_FP16;
   const CUtensorMapDataType tt =
       f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int rows = 128, half = fa::kBwdSub;
-  if (!encode_map(&mq, q, bhi, N, d, rows, tt) || !encode_map(&mk, k, bhi, N, d, rows, tt) ||
-      !encode_map(&mv, v, bhi, N, d, rows, tt) || !encode_map(&mdo, dout, bhi, N, d, rows, tt) ||
-      !encode_map(&mq64, q, bhi, N, d, half, tt) || !encode_map(&mk64, k, bhi, N, d, half, tt) ||
-      !encode_map(&mv64, v, bhi, N, d, half, tt) || !encode_map(&mdo64, dout, bhi, N, d, half, tt))
+  if (!encode_map4(&mq, q, tt, B, H, N, d, st[0], rows) ||
+      !encode_map4(&mk, k, tt, B, H, N, d, st[1], rows) ||
+      !encode_map4(&mv, v, tt, B, H, N, d, st[2], rows) ||
+      !encode_map4(&mdo, dout, tt, B, H, N, d, st[4], rows) ||
+      !encode_map4(&mq64, q, tt, B, H, N, d, st[0], half) ||
+      !encode_map4(&mk64, k, tt, B, H, N, d, st[1], half) ||
+      !encode_map4(&mv64, v, tt, B, H, N, d, st[2], half) ||
+      !encode_map4(&mdo64, dout, tt, B, H, N, d, st[4], half))
     return FA_ERR_LAUNCH;
 
   fa::BwdParams prm;
   prm.out0 = static_cast<uint16_t*>(dk);
+  prm.out0_sb = st[6][0];
+  prm.out0_sh = st[6][1];
+  prm.out0_sn = st[6][2];
   prm.out1 = static_cast<uint16_t*>(dv);
+  prm.out1_sb = st[7][0];
+  prm.out1_sh = st[7][1];
+  prm.out1_sn = st[7][2];
   float* ws = static_cast<float*>(workspace);
   prm.lse2 = ws;
   prm.dvec = ws + BH * Npad;
@@ -556,6 +595,7 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   prm.Npad = static_cast<int>(Npad);
   prm.T = static_cast<int>(T);
   prm.num_bh = static_cast<int>(BH);
+  prm.H = H;
   prm.causal = causal;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.scale = scale;
@@ -563,18 +603,46 @@ extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void
   prm.inject = g_inject.load(std::memory_order_relaxed);
   fa::BwdParams prm_q = prm;
   prm_q.out0 = static_cast<uint16_t*>(dq);
+  prm_q.out0_sb = st[5][0];
+  prm_q.out0_sh = st[5][1];
+  prm_q.out0_sn = st[5][2];
   prm_q.out1 = nullptr;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const BwdPrepIn pin{o, st[3], dout, st[4], lse};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const bool narrow = d <= 64;  // the D = 64 layout
   if (f16)
-    return narrow ? launch_bwd<64, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
-                                         prm, prm_q, sms, st)
-                  : launch_bwd<128, true>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
-                                          prm, prm_q, sms, st);
-  return narrow ? launch_bwd<64, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
-                                        prm, prm_q, sms, st)
-                : launch_bwd<128, false>(o, dout, lse, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64,
-                                         prm, prm_q, sms, st);
+    return narrow ? launch_bwd<64, true>(pin, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
+                                         prm_q, sms, cs)
+                  : launch_bwd<128, true>(pin, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
+                                          prm_q, sms, cs);
+  return narrow ? launch_bwd<64, false>(pin, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm, prm_q,
+                                        sms, cs)
+                : launch_bwd<128, false>(pin, mq, mk, mv, mdo, mq64, mk64, mv64, mdo64, prm,
+                                         prm_q, sms, cs);
+}
+
+}  // namespace
+
+extern "C" int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         int dtype, int B, int H, int N, int d, int causal, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, dout, nullptr, dq, nullptr,
+                  dk, nullptr, dv, nullptr, dtype, B, H, N, d, causal, scale, workspace,
+                  workspace_bytes, stream);
+}
+
+extern "C" int fa_bwd_strided(const void* q, const int64_t* q_strides, const void* k,
+                              const int64_t* k_strides, const void* v, const int64_t* v_strides,
+                              const void* o, const int64_t* o_strides, const float* lse,
+                              const void* dout, const int64_t* dout_strides, void* dq,
+                              const int64_t* dq_strides, void* dk, const int64_t* dk_strides,
+                              void* dv, const int64_t* dv_strides, int dtype, int B, int H, int N,
+                              int d, int causal, float scale, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, dout, dout_strides,
+                  dq, dq_strides, dk, dk_strides, dv, dv_strides, dtype, B, H, N, d, causal, scale,
+                  workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- host buffers (backward)

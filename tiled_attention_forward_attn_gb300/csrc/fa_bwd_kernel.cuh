@@ -10,6 +10,10 @@
 // (D_i equals sum_j P_ij dP_ij, the softmax Jacobian's correction term,
 // because O = P V.)
 //
+// Q, K, V, O, dO and the gradients are (batch, head, row, column) tensors at
+// caller strides (columns unit-stride), read through 4-D tensor maps {d, N,
+// H, B}; LSE and the workspace are contiguous.
+//
 // Three launches, no atomics:
 //   fa_bwd_prep_kernel    D and LSE * log2(e) per query row, into a
 //                         workspace padded to whole 128-row tiles;
@@ -71,8 +75,10 @@ constexpr int kBwdSub = 64;    // streamed rows per sub-step
 constexpr int kBwdEwCols = kBwdSub / 4;  // columns of a sub-step per elementwise warpgroup
 
 struct BwdParams {
-  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   [BH][N][d] bf16 or fp16
+  uint16_t* out0;     // key-tile pass: dK; query-tile pass: dQ   (b, h, row, col) bf16 or fp16
   uint16_t* out1;     // key-tile pass: dV; unused otherwise
+  int64_t out0_sb, out0_sh, out0_sn;  // element strides of out0 (batch, head, row; columns unit)
+  int64_t out1_sb, out1_sh, out1_sn;  // and of out1
   const float* lse2;  // [BH][Npad] -LSE * log2(e) per query (0 past N)
   const float* dvec;  // [BH][Npad] -rowsum(dO * O) per query (0 past N)
   int N;              // sequence length
@@ -80,6 +86,7 @@ struct BwdParams {
   int Npad;           // N rounded up to whole tiles
   int T;              // tiles per (batch, head) = Npad / 128
   int num_bh;         // B * H
+  int H;              // heads (bh = b * H + h)
   int causal;
   float scale_log2;   // scale * log2(e)
   float scale;        // the softmax scale
@@ -146,7 +153,9 @@ template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ lse2,
-                       float* __restrict__ dvec, int N, int Npad, int d) {
+                       float* __restrict__ dvec, int N, int Npad, int d, int H,
+                       int64_t o_sb, int64_t o_sh, int64_t o_sn, int64_t do_sb, int64_t do_sh,
+                       int64_t do_sn) {
   constexpr int kTpr = D / 8;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = gid / kTpr;  // padded row index bh * Npad + n
@@ -155,9 +164,11 @@ __global__ void __launch_bounds__(256)
   const int n = static_cast<int>(row - bh * Npad);
   float acc = 0.0f;
   if (n < N && part * 8 < d) {
-    const size_t off = (static_cast<size_t>(bh) * N + n) * d + part * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(o + off);
-    const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+    const int64_t bb = bh / H, hh = bh - bb * H;
+    const int64_t off_o = bb * o_sb + hh * o_sh + n * o_sn + part * 8;
+    const int64_t off_do = bb * do_sb + hh * do_sh + n * do_sn + part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + off_o);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + off_do);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -426,8 +437,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int live8 = (x_idx < p.N && guard(bh < p.num_bh && x_idx >= 0 && p.d <= D))
                             ? (p.d - kCols * part) / 8
                             : 0;
-      uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + x_idx) * p.d +
-                                            kCols * part);
+      const int ob = bh / p.H, oh = bh - ob * p.H;
+      const int64_t row_off = is_dv ? ob * p.out1_sb + oh * p.out1_sh + x_idx * p.out1_sn
+                                    : ob * p.out0_sb + oh * p.out0_sh + x_idx * p.out0_sn;
+      uint4* dst = reinterpret_cast<uint4*>(out + row_off + kCols * part);
 #pragma unroll
       for (int q8 = 0; q8 < kCols / 8; ++q8)
         if (q8 < live8) dst[q8] = make_uint4(w[4 * q8], w[4 * q8 + 1], w[4 * q8 + 2], w[4 * q8 + 3]);
@@ -454,10 +467,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!tma_coord_ok(64 * b, p.d, u.xt * kBwdTile, p.N, u.bh, p.num_bh) ||
               !smem_range_ok(C::kOffX + C::kTileBytes + b * kSwBlockBytes, kSwBlockBytes, C::kOffY))
             continue;
-          tma_load_3d_hint(sX + b * kSwBlockBytes, &tm_x0, bars.x_full(), 64 * b,
-                           u.xt * kBwdTile, u.bh, once);
-          tma_load_3d_hint(sX + C::kTileBytes + b * kSwBlockBytes, &tm_x1, bars.x_full(), 64 * b,
-                           u.xt * kBwdTile, u.bh, once);
+          tma_load_4d_hint(sX + b * kSwBlockBytes, &tm_x0, bars.x_full(), 64 * b,
+                           u.xt * kBwdTile, u.bh % p.H, u.bh / p.H, once);
+          tma_load_4d_hint(sX + C::kTileBytes + b * kSwBlockBytes, &tm_x1, bars.x_full(), 64 * b,
+                           u.xt * kBwdTile, u.bh % p.H, u.bh / p.H, once);
         }
         ++nx;
         for (int m = 0; m < 2 * u.steps; ++m, ++yc) {
@@ -482,10 +495,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 !smem_range_ok(C::kOffY + s * C::kStageBytes + C::kHalfBytes + b * C::kHalfBlock,
                                C::kHalfBlock, C::kOffVec))
               continue;
-            tma_load_3d_hint(stage + b * C::kHalfBlock, &tm_y0, bars.y_full(s), 64 * b, row0, u.bh,
-                             keep);
-            tma_load_3d_hint(stage + C::kHalfBytes + b * C::kHalfBlock, &tm_y1, bars.y_full(s),
-                             64 * b, row0, u.bh, keep);
+            tma_load_4d_hint(stage + b * C::kHalfBlock, &tm_y0, bars.y_full(s), 64 * b, row0,
+                             u.bh % p.H, u.bh / p.H, keep);
+            tma_load_4d_hint(stage + C::kHalfBytes + b * C::kHalfBlock, &tm_y1, bars.y_full(s),
+                             64 * b, row0, u.bh % p.H, u.bh / p.H, keep);
           }
           if (kKV && guard(row0 >= 0 && row0 + kBwdSub <= p.Npad && u.bh < p.num_bh) &&
               smem_range_ok(C::kOffVec + s * C::kVecBytes, C::kVecBytes, C::kOffBar)) {
