@@ -82,6 +82,7 @@ NCU_TRAFFIC_BYTES_DECODE = {
 # ncu capture; a workload is left out until a capture of the kernels as
 # benchmarked exists.
 NCU_TRAFFIC_BYTES_BWD = {
+    "b2h16n4096d128_causal": 436_226_816,
 }
 # Per-launch DRAM traffic of the forward kernel per workload, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left

@@ -148,7 +148,9 @@ struct BwdBars {
 
 // -D_i = -rowsum(dO_i * O_i) and -LSE_i * log2(e) for every row of the
 // padded [BH][Npad] layout (0 past N), negated for the elementwise pass's
-// fused multiply-adds.  D/8 threads per row, 16 bytes each.
+// fused multiply-adds.  D/8 threads per row, 16 bytes each; O and dO at
+// their element strides.  Row indices stay in 32 bits (the host rejects
+// BH * Npad above INT_MAX), so no thread pays for a 64-bit division.
 template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
@@ -156,19 +158,21 @@ __global__ void __launch_bounds__(256)
                        float* __restrict__ dvec, int N, int Npad, int d, int H,
                        int64_t o_sb, int64_t o_sh, int64_t o_sn, int64_t do_sb, int64_t do_sh,
                        int64_t do_sn) {
-  constexpr int kTpr = D / 8;
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = gid / kTpr;  // padded row index bh * Npad + n
-  const int part = static_cast<int>(gid % kTpr);
-  const int64_t bh = row / Npad;
-  const int n = static_cast<int>(row - bh * Npad);
+  constexpr int kTpr = D / 8;             // threads per row
+  constexpr int kRowsPerCta = 256 / kTpr;
+  const int row = static_cast<int>(blockIdx.x) * kRowsPerCta +
+                  static_cast<int>(threadIdx.x) / kTpr;  // padded row index bh * Npad + n
+  const int part = static_cast<int>(threadIdx.x) % kTpr;
+  const int bh = row / Npad;
+  const int n = row - bh * Npad;
   float acc = 0.0f;
   if (n < N && part * 8 < d) {
-    const int64_t bb = bh / H, hh = bh - bb * H;
+    const int bb = bh / H, hh = bh - bb * H;
     const int64_t off_o = bb * o_sb + hh * o_sh + n * o_sn + part * 8;
     const int64_t off_do = bb * do_sb + hh * do_sh + n * do_sn + part * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(o + off_o);
-    const uint4 b = *reinterpret_cast<const uint4*>(dout + off_do);
+    // Read once: streamed past L1.
+    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + off_o));
+    const uint4 b = __ldcs(reinterpret_cast<const uint4*>(dout + off_do));
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
