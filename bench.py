@@ -75,8 +75,8 @@ class L2Flush:
 # from one ncu capture per workload (profiles/); a workload is left out
 # until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES_DECODE = {
-    "decode_b4h16q16k16384d128_causal": 538_642_816,
-    "decode_b4h16q1k16384d128": 538_550_528,
+    "decode_b4h16q16k16384d128_causal": 538_348_715,
+    "decode_b4h16q1k16384d128": 538_085_120,
 }
 # DRAM bytes (read + write) of one backward step (three launches), from an
 # ncu capture; a workload is left out until a capture of the kernels as
@@ -89,7 +89,13 @@ NCU_TRAFFIC_BYTES_BWD = {
 # out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
     "b2h16n4096d128_causal": 136_679_936,
-    "b2h16n4096d256_causal": 575_434_624,
+    "b2h16n4096d256_causal": 575_460_352,
+    "b2h16n4096d128_causal_fp16": 135_673_941,
+    "b2h16n4096d96_causal": 77_866_752,
+    "b2h16n4096d64_causal": 50_821_376,
+    "b4h8n1024d64": 12_651_264,
+    "b1h16n16000d128_causal": 565_451_947,
+    "b1h32n8192d128_causal_qk3": 573_193_131,
 }
 
 
