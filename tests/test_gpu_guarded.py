@@ -13,6 +13,7 @@ import pytest
 import oracle
 import workloads
 from gpu_helpers import check_against_oracle, compare, to_device
+import test_gpu_random_sweep as sweep
 
 pytestmark = pytest.mark.gpu
 
@@ -142,4 +143,24 @@ def test_guarded_loop_order_ablation(fa, cuda_device, order):
                                                  True, scale, order)
     o_ref, lse_ref = oracle.attention(q, k, v, True, scale)
     compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"guarded order {order}")
+    _status_clean(fa)
+
+
+@pytest.mark.parametrize("case", sweep._fwd_cases()[:32], ids=lambda c: f"f{c[0]}")
+def test_guarded_random_forward(fa, cuda_device, case):
+    """The first cases of the random sweep (every layout, head dimension and
+    element type among them) with every access bounds-checked."""
+    sweep.test_forward_random_case(fa, cuda_device, case)
+    _status_clean(fa)
+
+
+@pytest.mark.parametrize("case", sweep._splitkv_cases()[:12], ids=lambda c: f"s{c[0]}")
+def test_guarded_random_splitkv(fa, cuda_device, case):
+    sweep.test_splitkv_random_case(fa, cuda_device, case)
+    _status_clean(fa)
+
+
+@pytest.mark.parametrize("case", sweep._bwd_cases()[:12], ids=lambda c: f"g{c[0]}")
+def test_guarded_random_backward(fa, cuda_device, case):
+    sweep.test_backward_random_case(fa, cuda_device, case)
     _status_clean(fa)

@@ -42,7 +42,7 @@ def _near_boundary_n(rng, hi):
     return int(rng.integers(1, hi))
 
 
-def _fwd_cases(n=40):
+def _fwd_cases(n=120):
     rng = np.random.Generator(np.random.PCG64(SEED))
     cases = []
     for i in range(n):
@@ -60,7 +60,7 @@ def _fwd_cases(n=40):
     return cases
 
 
-def _bwd_cases(n=16):
+def _bwd_cases(n=40):
     rng = np.random.Generator(np.random.PCG64(SEED + 1))
     cases = []
     for i in range(n):
@@ -75,7 +75,7 @@ def _bwd_cases(n=16):
     return cases
 
 
-def _splitkv_cases(n=16):
+def _splitkv_cases(n=40):
     rng = np.random.Generator(np.random.PCG64(SEED + 2))
     cases = []
     for i in range(n):
