@@ -336,6 +336,36 @@ def test_bwd_strided_validation(lib):
             assert call(st) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
 
 
+def test_strides_whose_span_overflows_are_rejected(lib):
+    """A stride times its extent is checked before it is formed: a batch
+    stride of 2^37 elements over 2^20 batches (a 2^57-element span) is
+    rejected with FA_ERR_STRIDE by the forward and the backward, instead of
+    wrapping around in 64-bit arithmetic; the same stride over 2 batches is
+    valid."""
+    import torch
+
+    big = 1 << 40
+    huge = (1 << 37, 64, 64)
+
+    def fwd(B, qs):
+        st = (ctypes.c_int64 * 3)(*qs)
+        return lib.fa_fwd_strided(big, st, 2 * big, None, 3 * big, None, 4 * big, None,
+                                  5 * big, 0, B, 1, 8, 64, 0, 0.1, None)
+
+    def bwd(B, qs):
+        st = (ctypes.c_int64 * 3)(*qs)
+        ptrs = [big * (i + 1) for i in range(8)]
+        return lib.fa_bwd_strided(ptrs[0], st, ptrs[1], None, ptrs[2], None, ptrs[3], None,
+                                  9 * big, ptrs[4], None, ptrs[5], None, ptrs[6], None,
+                                  ptrs[7], None, 0, B, 1, 8, 64, 0, 0.1, 10 * big, 1 << 30, None)
+
+    assert fwd(1 << 20, huge) == FA_ERR_STRIDE
+    assert bwd(1 << 20, huge) == FA_ERR_STRIDE
+    if not torch.cuda.is_available():
+        assert fwd(2, huge) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+        assert bwd(2, huge) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
+
+
 def test_fwd_host_validation(lib):
     """fa_fwd_host rejects bad arguments before queueing any copy (no GPU
     needed for these checks)."""

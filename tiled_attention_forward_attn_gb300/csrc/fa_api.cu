@@ -231,8 +231,24 @@ bool encode_map4(CUtensorMap* map, const void* ptr, CUtensorMapDataType type, in
   return r == CUDA_SUCCESS;
 }
 
+// Whether the element span of a strided [B][H][N][d] tensor stays below
+// 2^55 elements (64 PiB of 2-byte elements), so that every later span,
+// overlap and kernel address computation is exact in int64.  Each product is
+// checked before it is formed.
+bool span_in_range(int B, int H, int N, int d, const int64_t* st) {
+  constexpr int64_t kLimit = int64_t(1) << 55;
+  const int64_t ext[3] = {B, H, N};
+  int64_t total = d;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t n1 = ext[i] - 1;
+    if (n1 > 0 && st[i] > (kLimit - total) / n1) return false;
+    total += n1 * st[i];
+  }
+  return true;
+}
+
 // Bytes from the first to one past the last element of a strided
-// [B][H][N][d] tensor of 2-byte elements.
+// [B][H][N][d] tensor of 2-byte elements (span_in_range must hold).
 size_t span_bytes(int B, int H, int N, int d, const int64_t* st) {
   const int64_t last = (B - 1) * st[0] + (H - 1) * st[1] + (N - 1) * st[2] + d;
   return static_cast<size_t>(last) * 2;
@@ -282,9 +298,11 @@ int fwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* 
   const int64_t* ks = ks_in ? ks_in : contig;
   const int64_t* vs = vs_in ? vs_in : contig;
   const int64_t* os = os_in ? os_in : contig;
-  for (const int64_t* st : {qs, ks, vs, os})
+  for (const int64_t* st : {qs, ks, vs, os}) {
     for (int i = 0; i < 3; ++i)
       if (st[i] < 0 || st[i] % 8 != 0 || st[i] >= (int64_t(1) << 38)) return FA_ERR_STRIDE;
+    if (!span_in_range(B, H, N, d, st)) return FA_ERR_STRIDE;
+  }
   if (!strides_disjoint(B, H, N, d, os)) return FA_ERR_STRIDE;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) &
@@ -530,6 +548,7 @@ int bwd_impl(const void* q, const int64_t* qs_in, const void* k, const int64_t* 
     // D pre-pass and the gradient stores move as one 16-byte word) aligned.
     for (int i = 0; i < 3; ++i)
       if (s[i] < 0 || s[i] % 8 != 0 || s[i] >= (int64_t(1) << 38)) return FA_ERR_STRIDE;
+    if (!span_in_range(B, H, N, d, s)) return FA_ERR_STRIDE;
   }
   for (int i = 5; i < 8; ++i)
     if (!strides_disjoint(B, H, N, d, st[i])) return FA_ERR_STRIDE;
