@@ -366,6 +366,20 @@ def test_strides_whose_span_overflows_are_rejected(lib):
         assert bwd(2, huge) in (FA_ERR_LAUNCH, FA_ERR_DEVICE)
 
 
+def test_workspace_queries_return_zero_for_rejected_shapes(lib):
+    """Every size query answers 0, without overflowing, for a shape its entry
+    point rejects as too large."""
+    n = 1 << 30
+    assert lib.fa_bwd_workspace_bytes(n, n, n, 64) == 0
+    assert lib.fa_bwd_host_workspace_bytes(n, n, n, 64) == 0
+    assert lib.fa_fwd_host_workspace_bytes(n, n, n, 64) == 0
+    assert lib.fa_fwd_order_ablation_workspace_bytes(n, n, n, 64, 1) == 0
+    assert lib.fa_fwd_splitkv_workspace_bytes(n, n, 16, n, 64, 0) == 0
+    # and a shape just inside the limits still has a size
+    assert lib.fa_bwd_workspace_bytes(1, 1, 1 << 20, 64) == 2 * (1 << 20) * 4
+    assert lib.fa_fwd_order_ablation_workspace_bytes(1, 1, 1000, 64, 1) > 0
+
+
 def test_fwd_host_validation(lib):
     """fa_fwd_host rejects bad arguments before queueing any copy (no GPU
     needed for these checks)."""

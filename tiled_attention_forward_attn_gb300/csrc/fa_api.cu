@@ -400,6 +400,7 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 extern "C" size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0) return 0;
   if (d != 256 && (d < 16 || d > 128 || d % 16 != 0)) return 0;
+  if (static_cast<int64_t>(B) * H * N > INT_MAX) return 0;  // as fa_fwd_host rejects
   const size_t rows = static_cast<size_t>(B) * H * N;
   return 4 * round256(rows * d * 2) + round256(rows * 4);
 }
@@ -512,6 +513,7 @@ bool bwd_head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
 extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || !bwd_head_dim_ok(d)) return 0;
   const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH * bwd_npad(N) > INT_MAX) return 0;  // as the backward rejects
   return static_cast<size_t>(2 * BH * bwd_npad(N) * 4);
 }
 
@@ -766,7 +768,10 @@ int launch_order(int order, const CUtensorMap& mq, const CUtensorMap& mk, const 
 extern "C" size_t fa_fwd_order_ablation_workspace_bytes(int B, int H, int N, int d, int order) {
   if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || (order != 1 && order != 2)) return 0;
   if (order == 2) return 16;  // the v2 order keeps its state on chip
-  const int64_t rows = static_cast<int64_t>(B) * H * ord_npad(N);
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > 65535) return 0;  // as the call rejects
+  const int64_t rows = BH * ord_npad(N);
+  if (rows > INT_MAX / 4) return 0;
   return static_cast<size_t>(rows * (static_cast<int64_t>(d) + 2) * 4);
 }
 
