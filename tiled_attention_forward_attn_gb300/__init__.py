@@ -10,6 +10,7 @@ Also: :func:`fa_fwd_host` (the forward for tensors in host memory, copies
 included), :func:`fa_fwd_splitkv` / :func:`attention_forward_splitkv` (few
 queries against many keys) and :func:`fa_fwd_splitkv_static`,
 :func:`fa_bwd` / :func:`attention_backward` (gradients, bf16 or fp16),
+:func:`attention` (forward and backward as one torch.autograd function),
 :func:`fa_fwd_splitkv_host` and :func:`fa_bwd_host` (host tensors, copies included),
 :func:`attention_forward_order_ablation` (the two loop orders), and the
 device status / test-hook functions.  :func:`reload_library` switches to
@@ -33,7 +34,7 @@ __all__ = [
     "attention_forward_splitkv", "fa_fwd_splitkv_static", "fa_fwd_splitkv_static_scratch_bytes",
     "fa_fwd_splitkv_host", "fa_fwd_splitkv_host_workspace_bytes",
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_host", "fa_bwd_host_workspace_bytes",
-    "attention_backward", "attention_forward_order_ablation",
+    "attention_backward", "attention", "attention_forward_order_ablation",
     "fa_get_device_status", "fa_clear_device_status", "fa_set_wait_limit_ns",
     "fa_set_fault_injection", "load_library", "reload_library", "LIB_PATH", "GUARDED_LIB_PATH",
     "FA_DEVICE_STATUS_TIMEOUT", "FA_DEVICE_STATUS_BOUNDS", "FA_INJECT_SKIP_FIRST_V_LOAD",
@@ -565,6 +566,50 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, None, stream)
     return dq, dk, dv
+
+
+_autograd_fn = None
+
+
+def _attention_function():
+    """The torch.autograd.Function behind :func:`attention`, made on first use."""
+    global _autograd_fn
+    if _autograd_fn is None:
+        import torch
+
+        class AttentionFunction(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, causal, scale):
+                o, lse = attention_forward(q, k, v, causal=causal, scale=scale)
+                ctx.save_for_backward(q, k, v, o, lse)
+                ctx.causal, ctx.scale = causal, scale
+                return o
+
+            @staticmethod
+            def backward(ctx, grad_o):
+                q, k, v, o, lse = ctx.saved_tensors
+                # Autograd may hand over an expanded or otherwise strided
+                # gradient; the backward wants unit column stride and strides
+                # that are multiples of 8 elements.
+                ok = grad_o.dtype == q.dtype and grad_o.stride(3) == 1 and all(
+                    grad_o.shape[i] == 1 or grad_o.stride(i) % 8 == 0 for i in range(3))
+                dout = grad_o if ok else grad_o.to(q.dtype).contiguous()
+                dq, dk, dv = attention_backward(q, k, v, o, lse, dout, causal=ctx.causal,
+                                                scale=ctx.scale)
+                return dq, dk, dv, None, None
+
+        _autograd_fn = AttentionFunction
+    return _autograd_fn
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """Differentiable attention for PyTorch training code: the forward runs
+    :func:`fa_fwd` and keeps O and LSE; ``.backward()`` runs :func:`fa_bwd`
+    (head dimensions that are multiples of 16 up to 128 for the backward).
+    q, k, v: ``[B, H, N, d]`` CUDA tensors, bf16 or fp16.  Returns O."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(_dims(q)[3])
+    return _attention_function().apply(q, k, v, bool(causal), float(scale))
 
 
 def attention_forward_order_ablation(q, k, v, causal: bool, scale: float, order: int,
