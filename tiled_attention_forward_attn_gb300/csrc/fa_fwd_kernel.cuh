@@ -125,9 +125,9 @@ struct Cfg {
   static constexpr uint32_t kOffQ = 0;  // Q_A, Q_B
   static constexpr uint32_t kOffRing = kOffQ + kTilesPerCta * kQBytes;
   static constexpr uint32_t kOffBar = kOffRing + kSlots * kKVBytes;
-  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, p_half[2],
-  // kv_full[R], kv_empty[R], pv_half[2]
-  static constexpr int kNumBars = 15 + 2 * kSlots;
+  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, kv_full[R],
+  // kv_empty[R]
+  static constexpr int kNumBars = 11 + 2 * kSlots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -147,11 +147,8 @@ struct Barriers {
   __device__ uint32_t p_full(int t) const { return base + 48u + 8u * t; }
   __device__ uint32_t o_done(int t) const { return base + 64u + 8u * t; }
   __device__ uint32_t mma_done() const { return base + 80u; }
-  __device__ uint32_t p_half(int t) const { return base + 88u + 8u * t; }
-  __device__ uint32_t kv_full(int s) const { return base + 104u + 8u * s; }
-  __device__ uint32_t kv_empty(int s) const { return base + 104u + 8u * (slots + s); }
-  // Completion of the P.V MMAs of the first 64 keys of tile t's current key tile.
-  __device__ uint32_t pv_half(int t) const { return base + 104u + 8u * (2 * slots + t); }
+  __device__ uint32_t kv_full(int s) const { return base + 88u + 8u * s; }
+  __device__ uint32_t kv_empty(int s) const { return base + 88u + 8u * (slots + s); }
 };
 
 struct WaitCtx {
@@ -302,9 +299,7 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
 
     // P = 2^(s*c - m_ref) and its row sum; P_t goes, as 16-bit pairs, over the
     // first 64 columns of S_t (whose values are already in registers), in
-    // two halves of 64 keys, each handed over on its own (p_half, then
-    // p_full): the P.V MMAs of the first 64 keys start while the second half
-    // of P is still being computed.
+    // two halves of 64 keys, and is handed over once, whole (p_full).
     float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
     uint32_t pk[32];
     auto exps_half = [&](int h, float neg_m) {
@@ -372,8 +367,8 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
     // when a half's sum exceeds the limit (or is not finite), and always on
     // the first tile, where m_ref = -inf, is the reference moved to the true
     // maximum and the half computed again.
-    //   First half: nothing has been handed over yet, so the reference moves
-    //   for the whole tile (extreme of all 128 keys).
+    //   First half: the reference moves for the whole tile (extreme of all
+    //   128 keys).
     bool moved = j == 0;
     if (!moved) {
       exps_half(0, -m_ref);
@@ -386,24 +381,21 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
       m_ref = m_new;
       sa0 = sa1 = sb0 = sb1 = 0.f;
       exps_half(0, -m_ref);
-      tmem_st32(s_addr, pk);
       // O_t holds every P.V product up to tile j-1 (the S_t(j) MMA was
-      // committed after them) and no MMA touches it until p_half: rescale
-      // it in place, before the first half of P is handed over.
+      // committed after them) and no MMA touches it until p_full: rescale
+      // it in place.
       if (j > 0) rescale_o(alpha);
-    } else {
-      tmem_st32(s_addr, pk);
     }
-    tmem_st_wait();
-    tc_fence_before_sync();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bars.p_half(t));
-    l_run += (sa0 + sa1) + (sb0 + sb1);
+    tmem_st32(s_addr, pk);
+    float sum0 = (sa0 + sa1) + (sb0 + sb1);
 
-    //   Second half: after a move above every P of the tile is <= 1.  If the
-    //   sum still exceeds the limit, the first half is already in the P.V
-    //   MMAs: wait for them (pv_half), move the reference to the extreme of
-    //   the second half, rescale O_t and the running sum, recompute.
+    //   Second half: after a move above every P of the tile is <= 1.  If its
+    //   sum still exceeds the limit, the reference moves to the extreme of the
+    //   second half: O_t (which this tile's P.V, waiting for p_full, has not
+    //   touched yet) and the running sum are rescaled, the second half is
+    //   computed again, and the first half, already in TMEM, is scaled by the
+    //   same factor there (one more 16-bit rounding of those P, on this rare
+    //   path only), so that both halves of P share the new reference.
     sa0 = sa1 = sb0 = sb1 = 0.f;
     exps_half(1, -m_ref);
     if (__any_sync(0xffffffffu, !((sa0 + sa1) + (sb0 + sb1) <= kPSumLimit))) {
@@ -411,18 +403,28 @@ __device__ __forceinline__ bool softmax_tile(const int t, const int n_tiles, con
       const float alpha = ex2_approx(m_ref - m_new);
       l_run *= alpha;
       m_ref = m_new;
+      if (j > 0) rescale_o(alpha);
       sa0 = sa1 = sb0 = sb1 = 0.f;
       exps_half(1, -m_ref);
-      if (!warp_wait_bar(bars.pv_half(t), parity_of(s_uses - 1), wctx)) return false;
-      tc_fence_after_sync();
-      rescale_o(alpha);
+      tmem_st32(s_addr + 32, pk);
+      tmem_st_wait();
+      tmem_ld32(s_addr, pk);
+      tmem_ld_wait();
+      tmem_ld_fence(pk);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        pk[i] = pack_x2<kF16>(elem_to_f32<kF16>(pk[i], false) * alpha,
+                              elem_to_f32<kF16>(pk[i], true) * alpha);
+      tmem_st32(s_addr, pk);
+      sum0 *= alpha;
+    } else {
+      tmem_st32(s_addr + 32, pk);
     }
-    tmem_st32(s_addr + 32, pk);
     tmem_st_wait();
     tc_fence_before_sync();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bars.p_full(t));
-    l_run += (sa0 + sa1) + (sb0 + sb1);
+    l_run += sum0 + ((sa0 + sa1) + (sb0 + sb1));
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -494,8 +496,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.q_empty(t), 1);
       mbar_init(bars.s_full(t), 1);
       mbar_init(bars.p_full(t), kRowThreadsPerTile / 32);  // one arrival per warp
-      mbar_init(bars.p_half(t), kRowThreadsPerTile / 32);
-      mbar_init(bars.pv_half(t), 1);
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.mma_done(), 1);
@@ -726,19 +726,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int t = 0; t < kTilesPerCta; ++t) {
           const int n = t == 0 ? u.n[0] : u.n[1];
           if (!ok || j >= n) continue;
-          if (!warp_wait_bar(bars.p_half(t), parity_of(pc[t]), wctx)) {
-            ok = false;
-            continue;
-          }
-          tc_fence_after_sync();
-          issue_pv(t, v_slot, j == 0, 0);
-          commit(bars.pv_half(t));
           if (!warp_wait_bar(bars.p_full(t), parity_of(pc[t]), wctx)) {
             ok = false;
             continue;
           }
           ++pc[t];
           tc_fence_after_sync();
+          issue_pv(t, v_slot, j == 0, 0);
           issue_pv(t, v_slot, j == 0, 1);
           // V_j is free once the last tile that reads it has its P.V issued
           // (released before the S MMA that follows, to refill the ring early).
