@@ -126,8 +126,8 @@ struct Cfg {
   static constexpr uint32_t kOffRing = kOffQ + kTilesPerCta * kQBytes;
   static constexpr uint32_t kOffBar = kOffRing + kSlots * kKVBytes;
   // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, kv_full[R],
-  // kv_empty[R], pv_mark
-  static constexpr int kNumBars = 12 + 2 * kSlots;
+  // kv_empty[R]
+  static constexpr int kNumBars = 11 + 2 * kSlots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
   static constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -149,9 +149,6 @@ struct Barriers {
   __device__ uint32_t mma_done() const { return base + 80u; }
   __device__ uint32_t kv_full(int s) const { return base + 88u + 8u * s; }
   __device__ uint32_t kv_empty(int s) const { return base + 88u + 8u * (slots + s); }
-  // Committed between the two P.V halves of a tile and never waited on: the
-  // commit alone made the 64-column kernel's short P.V MMAs run faster.
-  __device__ uint32_t pv_mark() const { return base + 88u + 8u * (2 * slots); }
 };
 
 struct WaitCtx {
@@ -502,7 +499,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.mma_done(), 1);
-    mbar_init(bars.pv_mark(), 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(bars.kv_full(s), 1);
       mbar_init(bars.kv_empty(s), 1);
@@ -737,7 +733,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           ++pc[t];
           tc_fence_after_sync();
           issue_pv(t, v_slot, j == 0, 0);
-          commit(bars.pv_mark());
           issue_pv(t, v_slot, j == 0, 1);
           // V_j is free once the last tile that reads it has its P.V issued
           // (released before the S MMA that follows, to refill the ring early).
