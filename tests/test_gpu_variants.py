@@ -217,7 +217,8 @@ def _growing_scores(B, H, N, d, seed, dtype):
 def test_reference_moves_mid_tile(fa, cuda_device, d, causal, dtype):
     """Rows whose maximum grows inside a key tile (second half) and at the
     first half of the next, so the exponent reference moves after the first
-    half of P has been handed over: the result is still the oracle's."""
+    half of P has been computed and stored (that half is then rescaled in
+    place): the result is still the oracle's."""
     N = 1000
     scale = 0.125 if d == 64 else 1.0 / math.sqrt(d)
     q, k, v = _growing_scores(1, 2, N, d, seed=690 + d, dtype=dtype)
