@@ -88,14 +88,7 @@ NCU_TRAFFIC_BYTES_BWD = {
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
-    "b2h16n4096d128_causal": 137_150_379,
     "b2h16n4096d256_causal": 575_460_352,
-    "b2h16n4096d128_causal_fp16": 136_946_773,
-    "b2h16n4096d96_causal": 77_887_915,
-    "b2h16n4096d64_causal": 50_902_101,
-    "b4h8n1024d64": 12_651_947,
-    "b1h16n16000d128_causal": 556_244_651,
-    "b1h32n8192d128_causal_qk3": 575_374_421,
 }
 
 

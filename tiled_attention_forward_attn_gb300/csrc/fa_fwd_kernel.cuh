@@ -125,8 +125,8 @@ struct Cfg {
   static constexpr uint32_t kOffQ = 0;  // Q_A, Q_B
   static constexpr uint32_t kOffRing = kOffQ + kTilesPerCta * kQBytes;
   static constexpr uint32_t kOffBar = kOffRing + kSlots * kKVBytes;
-  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, kv_full[R],
-  // kv_empty[R]
+  // q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], mma_done, kv_full[R]
+  // (one per group of two ring items), kv_empty[R] (one per ring slot)
   static constexpr int kNumBars = 11 + 2 * kSlots;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16;
@@ -147,7 +147,13 @@ struct Barriers {
   __device__ uint32_t p_full(int t) const { return base + 48u + 8u * t; }
   __device__ uint32_t o_done(int t) const { return base + 64u + 8u * t; }
   __device__ uint32_t mma_done() const { return base + 80u; }
-  __device__ uint32_t kv_full(int s) const { return base + 88u + 8u * s; }
+  // Ring items i = 0, 1, 2, ... (K_0, V_0, K_1, V_1, ..., V_last, the next
+  // unit's K_0, ...) form groups g = (i + 1) / 2: {K_0}, {V_0, K_1}, ...,
+  // {V_last, next K_0}: exactly the items the MMA warp needs at one point.
+  // Group g completes phase g / slots of kv_full(g % slots) when both of its
+  // copies have landed (two arrivals; a group of one gets a plain second
+  // arrival), so the MMA warp waits once per key tile instead of twice.
+  __device__ uint32_t kv_full(int g) const { return base + 88u + 8u * g; }
   __device__ uint32_t kv_empty(int s) const { return base + 88u + 8u * (slots + s); }
 };
 
@@ -500,7 +506,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     mbar_init(bars.mma_done(), 1);
     for (int s = 0; s < R; ++s) {
-      mbar_init(bars.kv_full(s), 1);
+      mbar_init(bars.kv_full(s), 2);  // two items per group
       mbar_init(bars.kv_empty(s), 1);
     }
     *abort_flag = 0u;
@@ -560,22 +566,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (ic >= static_cast<uint32_t>(R) &&
             !wait_bar(bars.kv_empty(s), parity_of(ic / R - 1), wctx))
           return false;
+        const uint32_t full = bars.kv_full(static_cast<int>(((ic + 1) / 2) % R));
         if (skip) {
           skipped = ic;
         } else {
-          mbar_arrive_expect_tx(bars.kv_full(s), C::kKVBytes);
+          mbar_arrive_expect_tx(full, C::kKVBytes);
 #pragma unroll
           for (int b = 0; b < D / 64; ++b)
             if (tma_coord_ok(64 * b, p.d, row0, p.N, cur_b * p.H + cur_h, p.num_bh) &&
                 smem_range_ok(C::kOffRing + s * C::kKVBytes + b * kSwBlockBytes, kSwBlockBytes,
                               C::kOffBar))
-              tma_load_4d_hint(sRing + s * C::kKVBytes + b * kSwBlockBytes, map, bars.kv_full(s),
-                               64 * b, row0, cur_h, cur_b, keep);
+              tma_load_4d_hint(sRing + s * C::kKVBytes + b * kSwBlockBytes, map, full, 64 * b,
+                               row0, cur_h, cur_b, keep);
         }
         ++ic;
         return true;
       };
       bool ok = true;
+      // Group 0 holds K_0 of the first unit alone: its second arrival.
+      mbar_arrive(bars.kv_full(0));
       for (int r = 0; ok; ++r) {
         const int idx = unit_index(r);
         if (idx >= p.total_units) break;
@@ -611,17 +620,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ok = false;
         }
       }
+      // The last group holds one item when the item count is even (always,
+      // unless the loop stopped early): its second arrival.
+      if (ic > 0 && ic % 2 == 0) mbar_arrive(bars.kv_full(static_cast<int>((ic / 2) % R)));
       // Drain: every copy issued must land before the CTA may exit.  The last
-      // item in slot s is the largest count < ic congruent to s mod R.
+      // group on barrier x is the largest g <= ic / 2 congruent to x mod R; a
+      // group holding the skipped item (test hook) never completes, nor does
+      // any later group on its barrier.
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t)
         if (qc[t] > 0) wait_bar_drain(bars.q_full(t), parity_of(qc[t] - 1), wctx);
-      for (int s = 0; s < R; ++s) {
-        if (ic > static_cast<uint32_t>(s)) {
-          const uint32_t last = ic - 1 - ((ic - 1 - s) % R);
-          if (static_cast<int64_t>(last) != skipped)
-            wait_bar_drain(bars.kv_full(s), parity_of(last / R), wctx);
-        }
+      const uint32_t g_last = ic / 2;
+      const int64_t g_skip = skipped >= 0 ? (skipped + 1) / 2 : -1;
+      for (int x = 0; x < R; ++x) {
+        if (g_last < static_cast<uint32_t>(x)) continue;
+        const uint32_t g = g_last - ((g_last - x) % R);
+        if (g_skip >= 0 && g_skip % R == x && static_cast<uint32_t>(g_skip) <= g) continue;
+        wait_bar_drain(bars.kv_full(x), parity_of(g / R), wctx);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -695,8 +710,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (idx >= p.total_units) break;
       const Unit u = unit_at(idx, p);
       const int n_max = max(u.n[0], u.n[1]);
-      // j = 0: S_t(0) for every active tile.
-      if (!warp_wait_bar(bars.kv_full(ic % R), parity_of(ic / R), wctx)) break;
+      // j = 0: S_t(0) for every active tile.  K_0 is in the group of the
+      // previous unit's last V, already waited for, except in the first unit.
+      if (ic == 0 && !warp_wait_bar(bars.kv_full(0), 0, wctx)) break;
       const uint32_t k0_slot = ic % R;
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t) {
@@ -717,8 +733,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const bool more = j + 1 < n_max;
         // Items ic (V_j) and ic + 1 (K_j+1, when there is one).
         const uint32_t v_slot = ic % R, k_slot = (ic + 1) % R;
-        if (!warp_wait_bar(bars.kv_full(v_slot), parity_of(ic / R), wctx) ||
-            (more && !warp_wait_bar(bars.kv_full(k_slot), parity_of((ic + 1) / R), wctx))) {
+        // One wait covers V_j and the item after it (K_j+1, or the next unit's K_0).
+        const uint32_t grp = (ic + 1) / 2;
+        if (!warp_wait_bar(bars.kv_full(static_cast<int>(grp % R)), parity_of(grp / R), wctx)) {
           ok = false;
           break;
         }
