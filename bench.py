@@ -88,7 +88,14 @@ NCU_TRAFFIC_BYTES_BWD = {
 # capture (dram__bytes_read.sum + dram__bytes_write.sum); a workload is left
 # out until a capture of the kernel as benchmarked exists.
 NCU_TRAFFIC_BYTES = {
+    "b2h16n4096d128_causal": 137_546_752,
     "b2h16n4096d256_causal": 575_460_352,
+    "b2h16n4096d128_causal_fp16": 137_477_973,
+    "b2h16n4096d96_causal": 77_837_909,
+    "b2h16n4096d64_causal": 50_824_704,
+    "b4h8n1024d64": 12_651_179,
+    "b1h16n16000d128_causal": 560_115_371,
+    "b1h32n8192d128_causal_qk3": 574_306_987,
 }
 
 
