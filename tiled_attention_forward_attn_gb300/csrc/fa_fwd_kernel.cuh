@@ -20,8 +20,13 @@
 //   warps 4-7   softmax and epilogue of tile B
 //   warp 8      TMA producer of Q_A, Q_B and of one K/V ring that it fills
 //               in the order the MMAs read it: K_0, then V_j, K_j+1 per key
-//               tile (each tile is prefetched about two iterations ahead)
-//   warp 9      TMEM allocator and the tcgen05.mma issuer
+//               tile (each tile is prefetched about two iterations ahead);
+//               V_j and K_j+1 complete one barrier phase together, so the
+//               issuer waits for the ring once per key tile
+//   warp 9      TMEM allocator and the tcgen05.mma issuer: its instruction
+//               stream bounds the kernel, so it waits as little as possible
+//               (per key tile: the K/V pair and each tile's P, handed over
+//               once, whole)
 //   warps 10-11 idle (they complete the third warpgroup)
 // The third warpgroup hands most of its registers to the two softmax
 // warpgroups (setmaxnreg): 384 threads launch with 168 registers each
